@@ -1,0 +1,220 @@
+// common.cuh -- device helpers and internal launch interfaces shared by the
+// translation units of libsparseopt (sm_103a).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sparseopt.h"
+
+namespace so {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kBlock = 256;            // threads per block of every kernel here
+constexpr int kPieceLen = 32;          // L: sorted entries summed by one team before a partial
+constexpr int kGroup = 32;             // G: fan-in of the partial-combining tree
+constexpr int kSortItems = 8;          // keys per thread in a radix pass
+constexpr int kSortTile = kBlock * kSortItems;
+constexpr int kRunItems = 8;           // sorted entries per thread in run detection
+constexpr int kRunTile = kBlock * kRunItems;
+constexpr int kMaxPasses = 4;          // 8-bit digits, keys < 2^32
+constexpr uint32_t kSingleMask = 0x7fffffffu;
+constexpr uint32_t kMultiFlag = 0x80000000u;
+// Bounded waits on another block's published value: after this many polls the
+// waiting block records SPARSE_ERR_INTERNAL and carries on with a zero value.
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+// ------------------------------------------------------------------ errors
+__device__ __forceinline__ void set_error(int32_t* d_err, int code)
+{
+    atomicCAS(d_err, 0, code);
+}
+
+__device__ __forceinline__ int read_error(const int32_t* d_err)
+{
+    return *reinterpret_cast<const volatile int32_t*>(d_err);
+}
+
+// ------------------------------------------------------- relaxed gpu-scope I/O
+__device__ __forceinline__ uint32_t ld_volatile(const uint32_t* p)
+{
+    return *reinterpret_cast<const volatile uint32_t*>(p);
+}
+__device__ __forceinline__ unsigned long long ld_volatile(const unsigned long long* p)
+{
+    return *reinterpret_cast<const volatile unsigned long long*>(p);
+}
+__device__ __forceinline__ void st_volatile(uint32_t* p, uint32_t v)
+{
+    *reinterpret_cast<volatile uint32_t*>(p) = v;
+}
+__device__ __forceinline__ void st_volatile(unsigned long long* p, unsigned long long v)
+{
+    *reinterpret_cast<volatile unsigned long long*>(p) = v;
+}
+
+// ------------------------------------------------- error-free transformation
+// Knuth's TwoSum: s + x = t + e exactly, t = fl(s + x).  Rounding-mode explicit
+// intrinsics keep the compiler from contracting or reassociating.
+__device__ __forceinline__ void two_sum_acc(float& s, float& c, float x)
+{
+    const float t = __fadd_rn(s, x);
+    const float bp = __fsub_rn(t, s);
+    const float e = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(x, bp));
+    s = t;
+    c = __fadd_rn(c, e);
+}
+
+// (s, c) += (s2, c2), both compensated pairs.
+__device__ __forceinline__ void two_sum_merge(float& s, float& c, float s2, float c2)
+{
+    two_sum_acc(s, c, s2);
+    c = __fadd_rn(c, c2);
+}
+
+// --------------------------------------------------------------- warp scans
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, x, d);
+        if (lane >= d) x += y;
+    }
+    return x;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x)
+{
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) x += __shfl_xor_sync(kFull, x, d);
+    return x;
+}
+
+// Exclusive scan of one uint32 per thread over a kBlock-thread block.
+// `tmp` is shared scratch of kBlock/32 + 1 words.  Returns the exclusive
+// prefix; *total receives the block sum.  Every thread of the block must call.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* tmp, uint32_t* total)
+{
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t incl = warp_incl_scan(x, lane);
+    if (lane == 31) tmp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < kBlock / 32 ? tmp[lane] : 0u;
+        const uint32_t wi = warp_incl_scan(w, lane);
+        if (lane < kBlock / 32) tmp[lane] = wi - w;
+        if (lane == kBlock / 32 - 1) tmp[kBlock / 32] = wi;
+    }
+    __syncthreads();
+    const uint32_t res = tmp[warp] + incl - x;
+    *total = tmp[kBlock / 32];
+    __syncthreads();
+    return res;
+}
+
+// ------------------------------------------------------------ workspace map
+struct WsLayout {
+    int64_t n, c, nb;
+    int passes, sort_tiles, run_tiles, levels;
+    size_t keys0, keys1, vals0, vals1, rec, seg_off, part;
+    size_t ctrl_begin, gh, counts, rstatus, dstatus, lvl_cnt, ctrl_end;
+    size_t total;
+};
+
+// counts[] word indices
+enum { kCtrHist = 0, kCtrPass0 = 1, kCtrRun = 5, kCntU = 8, kCntP = 9, kCountsWords = 16 };
+
+WsLayout ws_layout(int64_t n, int64_t c, int64_t bound);
+
+// Device pointers carved out of a workspace.
+struct SortWs {
+    uint32_t* keys[2];
+    uint32_t* vals[2];
+    uint4* rec;           // [P+1] piece records {start, key, u | multi, perm of start}
+    uint32_t* seg_off;    // [U+1]
+    float* part;          // partial sums: [2*nb slots][2][c]
+    uint32_t* gh;         // [4][256] digit histograms
+    uint32_t* counts;     // [16]
+    uint32_t* rstatus;    // [passes][sort_tiles][256]
+    unsigned long long* dstatus;  // [run_tiles]
+    uint32_t* lvl_cnt;    // [levels][2*nb]
+    int final_buf;        // which keys/vals buffer holds the sorted result
+};
+
+SortWs carve(const WsLayout& L, void* ws);
+
+// ------------------------------------------------------------ launch helpers
+int num_sms();
+
+// Sorts the keys (uint32 of idx) stably with their positions and detects runs.
+// Afterwards: ws.rec / ws.seg_off / counts[kCntU], counts[kCntP] describe the
+// segments; optional int64 outputs (idx_out, seg_off_out, perm_out, d_nnz_out)
+// are filled for sparse_canonicalize.  When ls != nullptr, each unique key k
+// (a row) is checked for ls[k] < t (per row) or ls[k*c + j] < t (per coord).
+cudaError_t sort_and_segment(const int64_t* idx, int64_t n, int64_t c, int64_t bound,
+                             const WsLayout& L, SortWs& ws, int64_t* idx_out,
+                             int64_t* seg_off_out, int64_t* perm_out, int64_t* d_nnz_out,
+                             const int64_t* ls, int ls_per_coord, int64_t t, int32_t* d_err,
+                             cudaStream_t s);
+
+// Checks a canonical row-COO: 0 <= rows[i] < r, strictly ascending, last_step < t.
+cudaError_t check_canonical_rows(const int64_t* rows, int64_t n, int64_t r, int64_t c,
+                                 const int64_t* ls, int ls_per_coord, int64_t t,
+                                 int32_t* d_err, cudaStream_t s);
+
+// ------------------------------------------------------- update parameters
+struct AdamParams {
+    float* p;
+    float* m;
+    float* v;
+    int64_t* ls;
+    int ls_per_coord;
+    int dd;               // DormancyDecay
+    int64_t t;
+    float beta1, beta2;   // decay factors
+    float omb1, omb2;     // 1 - beta
+    float log2b1, log2b2; // log2(beta) (-inf for beta = 0)
+    float inv_bc1, inv_bc2;  // 1 / (1 - beta^t)
+    float lr, eps;
+};
+
+struct SgdParams {
+    float* p;
+    float* buf;
+    float lr, momentum, wd;
+};
+
+struct StoreParams {
+    float* out;           // [U][c]
+};
+
+// Row-fused update from sorted segments (raw input) or canonical rows.
+cudaError_t fused_rows_adam_sorted(const SortWs& ws, const WsLayout& L, const float* vals, int64_t c,
+                                   const AdamParams& P, int vec4, int32_t* d_err, cudaStream_t s);
+cudaError_t fused_rows_adam_canon(const int64_t* rows, int64_t n, const float* vals, int64_t c,
+                                  const AdamParams& P, int vec4, int32_t* d_err, cudaStream_t s);
+cudaError_t fused_rows_sgd_sorted(const SortWs& ws, const WsLayout& L, const float* vals, int64_t c,
+                                  const SgdParams& P, int vec4, int32_t* d_err, cudaStream_t s);
+cudaError_t fused_rows_sgd_canon(const int64_t* rows, int64_t n, const float* vals, int64_t c,
+                                 const SgdParams& P, int vec4, int32_t* d_err, cudaStream_t s);
+cudaError_t fused_rows_store_sorted(const SortWs& ws, const WsLayout& L, const float* vals, int64_t c,
+                                    const StoreParams& P, int vec4, int32_t* d_err, cudaStream_t s);
+
+// CSR (element-granular) paths.
+cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, int64_t c, int64_t nnz,
+                      int full_rows, const int64_t* ls, int ls_per_coord, int64_t t, int32_t* d_err,
+                      cudaStream_t s);
+cudaError_t csr_adam(const int64_t* row_off, const int32_t* cols, const float* vals, int64_t r,
+                     int64_t c, int64_t nnz, const AdamParams& P, int32_t* d_err, cudaStream_t s);
+cudaError_t csr_sgd(const int64_t* row_off, const int32_t* cols, const float* vals, int64_t r,
+                    int64_t c, int64_t nnz, const SgdParams& P, int32_t* d_err, cudaStream_t s);
+cudaError_t csr_to_coo(const int64_t* row_off, const int32_t* cols, int64_t r, int64_t c,
+                       int64_t nnz, int64_t* lin_out, int32_t* d_err, cudaStream_t s);
+cudaError_t coo_to_csr(const int64_t* lin, int64_t nnz, int64_t r, int64_t c, int64_t* row_off_out,
+                       int32_t* cols_out, int32_t* d_err, cudaStream_t s);
+cudaError_t row_coo_to_csr(const int64_t* rows, int64_t nrows, int64_t r, int64_t c,
+                           int64_t* row_off_out, int32_t* cols_out, int32_t* d_err, cudaStream_t s);
+
+}  // namespace so

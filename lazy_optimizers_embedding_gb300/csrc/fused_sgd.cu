@@ -1,0 +1,20 @@
+// fused_sgd.cu -- lazy SGD (coupled weight decay, lazy momentum) row-fused
+// launches.  "Module sparse_optimizer" (optirs-gpu 0.3.2 docs), "Sparse SGD".
+#include "fused.cuh"
+
+namespace so {
+
+cudaError_t fused_rows_sgd_sorted(const SortWs& ws, const WsLayout& L, const float* vals, int64_t c,
+                                  const SgdParams& P, int vec4, int32_t* d_err, cudaStream_t s)
+{
+    return launch_fused(sorted_src(ws), L.n + L.nb, vals, c, SgdEpi{P, c}, ws.part, ws.lvl_cnt, L.nb, vec4,
+                        d_err, s);
+}
+
+cudaError_t fused_rows_sgd_canon(const int64_t* rows, int64_t n, const float* vals, int64_t c,
+                                 const SgdParams& P, int vec4, int32_t* d_err, cudaStream_t s)
+{
+    return launch_fused(CanonSrc{rows, n}, n, vals, c, SgdEpi{P, c}, nullptr, nullptr, 0, vec4, d_err, s);
+}
+
+}  // namespace so

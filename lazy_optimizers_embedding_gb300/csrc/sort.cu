@@ -1,0 +1,484 @@
+// sort.cu -- canonicalisation front half on the device:
+//   K1 range check + digit histograms of every radix pass,
+//   K2 stable LSD radix sort of (key, position), one 8-bit digit per pass,
+//      single-sweep per pass with decoupled look-back between tiles,
+//   K3 run detection: segment heads (key changes) and piece heads (segment heads
+//      plus every kPieceLen-th sorted position), compacted by a block scan with
+//      decoupled look-back.
+// Canonical form per "Module sparse_optimizer" (optirs-gpu 0.3.2 docs),
+// "Sparse gradient representations" (strictly ascending indices); sorting and
+// duplicate detection per the "DiskSparseAdam (DSA)" README, "Safe Duplicate
+// Aggregation & Sorted I/O".
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+#include "profile.cuh"
+
+namespace so {
+
+int num_sms()
+{
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    return sms;
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static int key_bits(int64_t bound)
+{
+    int b = 1;
+    while (b < 32 && (int64_t(1) << b) < bound) ++b;
+    return b;
+}
+
+WsLayout ws_layout(int64_t n, int64_t c, int64_t bound)
+{
+    WsLayout L{};
+    if (n < 1) n = 1;
+    if (c < 1) c = 1;
+    L.n = n;
+    L.c = c;
+    L.nb = (n + kPieceLen - 1) / kPieceLen;
+    L.passes = (key_bits(bound) + 7) / 8;
+    L.sort_tiles = (int)((n + kSortTile - 1) / kSortTile);
+    L.run_tiles = (int)((n + kRunTile - 1) / kRunTile);
+    int levels = 1;
+    for (int64_t k = L.nb + 1; k > 1; k = (k + kGroup - 1) / kGroup) ++levels;
+    L.levels = levels;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        off = align_up(off, 256);
+        size_t at = off;
+        off += bytes;
+        return at;
+    };
+    L.keys0 = take(sizeof(uint32_t) * n);
+    L.keys1 = take(sizeof(uint32_t) * n);
+    L.vals0 = take(sizeof(uint32_t) * n);
+    L.vals1 = take(sizeof(uint32_t) * n);
+    L.rec = take(sizeof(uint4) * (size_t)(n + L.nb + 2));
+    L.seg_off = take(sizeof(uint32_t) * (size_t)(n + 1));
+    L.part = take(sizeof(float) * (size_t)(2 * L.nb) * 2 * (size_t)c);
+    off = align_up(off, 256);
+    L.ctrl_begin = off;
+    L.gh = take(sizeof(uint32_t) * kMaxPasses * 256);
+    L.counts = take(sizeof(uint32_t) * kCountsWords);
+    L.rstatus = take(sizeof(uint32_t) * (size_t)L.passes * L.sort_tiles * 256);
+    L.dstatus = take(sizeof(unsigned long long) * (size_t)L.run_tiles);
+    L.lvl_cnt = take(sizeof(uint32_t) * (size_t)L.levels * 2 * L.nb);
+    L.ctrl_end = align_up(off, 256);
+    L.total = L.ctrl_end;
+    return L;
+}
+
+SortWs carve(const WsLayout& L, void* ws)
+{
+    char* b = static_cast<char*>(ws);
+    SortWs w{};
+    w.keys[0] = reinterpret_cast<uint32_t*>(b + L.keys0);
+    w.keys[1] = reinterpret_cast<uint32_t*>(b + L.keys1);
+    w.vals[0] = reinterpret_cast<uint32_t*>(b + L.vals0);
+    w.vals[1] = reinterpret_cast<uint32_t*>(b + L.vals1);
+    w.rec = reinterpret_cast<uint4*>(b + L.rec);
+    w.seg_off = reinterpret_cast<uint32_t*>(b + L.seg_off);
+    w.part = reinterpret_cast<float*>(b + L.part);
+    w.gh = reinterpret_cast<uint32_t*>(b + L.gh);
+    w.counts = reinterpret_cast<uint32_t*>(b + L.counts);
+    w.rstatus = reinterpret_cast<uint32_t*>(b + L.rstatus);
+    w.dstatus = reinterpret_cast<unsigned long long*>(b + L.dstatus);
+    w.lvl_cnt = reinterpret_cast<uint32_t*>(b + L.lvl_cnt);
+    w.final_buf = (L.passes - 1) & 1;
+    return w;
+}
+
+// ---------------------------------------------------------------------- K1
+// Range check (0 <= idx < bound) and the digit histograms of all passes.  Every
+// key is counted, valid or not, with the same truncation the radix passes use,
+// so the scatter offsets stay inside [0, n) whatever the input.
+__global__ void __launch_bounds__(kBlock) k_range_hist(const int64_t* __restrict__ idx, uint32_t n,
+                                                       int64_t bound, int passes,
+                                                       uint32_t* __restrict__ gh, int32_t* d_err)
+{
+    __shared__ uint32_t sh[kMaxPasses * 256];
+    for (int i = threadIdx.x; i < kMaxPasses * 256; i += kBlock) sh[i] = 0;
+    __syncthreads();
+    int bad = 0;
+    const uint32_t stride = gridDim.x * kBlock;
+    for (uint32_t i = blockIdx.x * kBlock + threadIdx.x; i < n; i += stride) {
+        const int64_t k = idx[i];
+        bad |= (k < 0) | (k >= bound);
+        const uint32_t key = static_cast<uint32_t>(static_cast<uint64_t>(k));
+        for (int p = 0; p < passes; ++p) atomicAdd(&sh[p * 256 + ((key >> (8 * p)) & 255u)], 1u);
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) set_error(d_err, SPARSE_ERR_INDEX_OUT_OF_RANGE);
+    for (int i = threadIdx.x; i < passes * 256; i += kBlock) {
+        const uint32_t v = sh[i];
+        if (v) atomicAdd(gh + i, v);
+    }
+}
+
+// ---------------------------------------------------------------------- K2
+// One stable counting pass over digit (key >> shift) & 255.  Tiles are taken in
+// launch order from an atomic counter, so a tile only ever waits on tiles that
+// are already running.  Per tile:
+//   1. warp-level ranking with __match_any_sync (warp w owns a contiguous run of
+//      the tile, items in order, so ranks are stable);
+//   2. per-digit tile counts are published (flag 1 = aggregate), the exclusive
+//      prefix over earlier tiles is found by look-back and republished
+//      (flag 2 = inclusive); status word = count << 2 | flag;
+//   3. the tile is reordered by digit in shared memory and written out, each
+//      digit's run landing contiguously at its global offset.
+template <bool kFirst>
+__global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict__ idx64,
+                                                       const uint32_t* __restrict__ kin,
+                                                       const uint32_t* __restrict__ vin,
+                                                       uint32_t* __restrict__ kout,
+                                                       uint32_t* __restrict__ vout, uint32_t n, int shift,
+                                                       const uint32_t* __restrict__ gh,
+                                                       uint32_t* status, uint32_t* tile_ctr,
+                                                       int32_t* d_err)
+{
+    constexpr int kWarps = kBlock / 32;
+    __shared__ uint32_t s_wh[kWarps][256];
+    __shared__ uint32_t s_gbase[256];
+    __shared__ uint32_t s_texcl[256];
+    __shared__ uint32_t s_scan[kWarps + 1];
+    __shared__ uint32_t s_keys[kSortTile];
+    __shared__ uint32_t s_vals[kSortTile];
+    __shared__ uint32_t s_tile;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    if (tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
+    for (int i = tid; i < kWarps * 256; i += kBlock) (&s_wh[0][0])[i] = 0u;
+    __syncthreads();
+    const uint32_t tile = s_tile;
+    const uint32_t base = tile * kSortTile;
+    const uint32_t tile_n = min(static_cast<uint32_t>(kSortTile), n - base);
+
+    uint32_t key[kSortItems], val[kSortItems], rank[kSortItems];
+    int dig[kSortItems];
+#pragma unroll
+    for (int i = 0; i < kSortItems; ++i) {
+        const uint32_t local = warp * 32 * kSortItems + i * 32 + lane;
+        const bool valid = local < tile_n;
+        uint32_t k = 0, v = 0;
+        if (valid) {
+            const uint32_t pos = base + local;
+            if (kFirst) {
+                k = static_cast<uint32_t>(static_cast<uint64_t>(idx64[pos]));
+                v = pos;
+            } else {
+                k = kin[pos];
+                v = vin[pos];
+            }
+        }
+        key[i] = k;
+        val[i] = v;
+        dig[i] = valid ? static_cast<int>((k >> shift) & 255u) : 256;
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < kSortItems; ++i) {
+        const int d = dig[i];
+        const uint32_t peers = __match_any_sync(kFull, d);
+        uint32_t b = 0;
+        if (d < 256) b = s_wh[warp][d];
+        __syncwarp();
+        if (d < 256 && lane == __ffs(peers) - 1) s_wh[warp][d] = b + __popc(peers);
+        __syncwarp();
+        rank[i] = b + __popc(peers & lt);
+    }
+    __syncthreads();
+
+    // thread tid owns digit tid
+    uint32_t run = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t cnt = s_wh[w][tid];
+        s_wh[w][tid] = run;
+        run += cnt;
+    }
+    const uint32_t tcount = run;
+    uint32_t* my = status + static_cast<size_t>(tile) * 256 + tid;
+    st_volatile(my, (tcount << 2) | (tile == 0 ? 2u : 1u));
+
+    uint32_t total;
+    s_texcl[tid] = block_excl_scan(tcount, s_scan, &total);
+    const uint32_t gexcl = block_excl_scan(gh[tid], s_scan, &total);
+
+    uint32_t excl = 0;
+    if (tile > 0) {
+        int64_t j = static_cast<int64_t>(tile) - 1;
+        uint32_t spins = 0;
+        while (j >= 0) {
+            const uint32_t w = ld_volatile(status + static_cast<size_t>(j) * 256 + tid);
+            const uint32_t flag = w & 3u;
+            if (flag == 0u) {
+                if (++spins > kSpinLimit) {
+                    set_error(d_err, SPARSE_ERR_INTERNAL);
+                    break;
+                }
+                if (spins > 64) __nanosleep(64);
+                continue;
+            }
+            excl += w >> 2;
+            if (flag == 2u) break;
+            --j;
+        }
+        st_volatile(my, ((excl + tcount) << 2) | 2u);
+    }
+    s_gbase[tid] = gexcl + excl;
+    __syncthreads();
+
+#pragma unroll
+    for (int i = 0; i < kSortItems; ++i) {
+        const int d = dig[i];
+        if (d < 256) {
+            const uint32_t lp = s_texcl[d] + s_wh[warp][d] + rank[i];
+            s_keys[lp] = key[i];
+            s_vals[lp] = val[i];
+        }
+    }
+    __syncthreads();
+    for (uint32_t i = tid; i < tile_n; i += kBlock) {
+        const uint32_t k = s_keys[i];
+        const uint32_t d = (k >> shift) & 255u;
+        const uint32_t dst = s_gbase[d] + (i - s_texcl[d]);
+        kout[dst] = k;
+        vout[dst] = s_vals[i];
+    }
+}
+
+// ---------------------------------------------------------------------- K3
+// Run detection over the sorted keys.  Position q is a segment head when it is
+// the first position or its key differs from the previous one; it is a piece
+// head when it is a segment head or q % kPieceLen == 0.  Each piece covers at
+// most kPieceLen sorted entries of one segment.  Outputs (u = segment index,
+// j = piece index):
+//   seg_off[u] = first sorted position of segment u, seg_off[U] = n
+//   rec[j] = {start, key, u | kMultiFlag if the segment spans several pieces,
+//             input position of the start}, rec[P] = {n, 0, 0, 0}
+// Status word of a tile: flag << 62 | heads << 31 | pieces.
+__global__ void __launch_bounds__(kBlock) k_run_detect(
+    const uint32_t* __restrict__ skey, const uint32_t* __restrict__ sperm, uint32_t n,
+    uint4* __restrict__ rec, uint32_t* __restrict__ seg_off, unsigned long long* dstatus,
+    uint32_t* tile_ctr, uint32_t* counts, int64_t* __restrict__ idx_out,
+    int64_t* __restrict__ seg_off_out, int64_t* __restrict__ perm_out, int64_t* d_nnz_out,
+    const int64_t* __restrict__ ls, int ls_per_coord, int64_t c, int64_t bound, int64_t t,
+    int32_t* d_err)
+{
+    constexpr unsigned long long kValMask = (1ull << 62) - 1ull;
+    __shared__ uint32_t s_scan[kBlock / 32 + 1];
+    __shared__ unsigned long long s_excl;
+    __shared__ uint32_t s_tile;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    if (tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
+    __syncthreads();
+    const uint32_t tile = s_tile;
+    const uint32_t p0 = tile * kRunTile + tid * kRunItems;
+
+    uint32_t k[kRunItems];
+    uint32_t prev = 0;
+    if (p0 < n && p0 > 0) prev = skey[p0 - 1];
+    if (p0 + kRunItems <= n) {
+        const uint4 a = *reinterpret_cast<const uint4*>(skey + p0);
+        const uint4 b = *reinterpret_cast<const uint4*>(skey + p0 + 4);
+        k[0] = a.x; k[1] = a.y; k[2] = a.z; k[3] = a.w;
+        k[4] = b.x; k[5] = b.y; k[6] = b.z; k[7] = b.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < kRunItems; ++i) k[i] = (p0 + i < n) ? skey[p0 + i] : 0u;
+    }
+    uint32_t headm = 0, piecem = 0;
+#pragma unroll
+    for (int i = 0; i < kRunItems; ++i) {
+        const uint32_t q = p0 + i;
+        if (q < n) {
+            const uint32_t before = (i == 0) ? prev : k[i - 1];
+            const bool h = (q == 0) || (k[i] != before);
+            headm |= (h ? 1u : 0u) << i;
+            piecem |= ((h || (q % kPieceLen) == 0) ? 1u : 0u) << i;
+        }
+    }
+    const uint32_t hc = __popc(headm), pc = __popc(piecem);
+    uint32_t tot;
+    const uint32_t xe = block_excl_scan((hc << 16) | pc, s_scan, &tot);
+    const unsigned long long agg = (static_cast<unsigned long long>(tot >> 16) << 31) | (tot & 0xffffu);
+
+    if (tid < 32) {
+        unsigned long long excl = 0;
+        if (tile == 0) {
+            if (lane == 0) st_volatile(dstatus + tile, (2ull << 62) | agg);
+        } else {
+            if (lane == 0) st_volatile(dstatus + tile, (1ull << 62) | agg);
+            int64_t top = static_cast<int64_t>(tile) - 1;
+            uint32_t spins = 0;
+            while (true) {
+                const int64_t jj = top - lane;
+                unsigned long long w = (jj >= 0) ? ld_volatile(dstatus + jj) : (2ull << 62);
+                while (__any_sync(kFull, (w >> 62) == 0ull)) {
+                    if (++spins > kSpinLimit) {
+                        if ((w >> 62) == 0ull) {
+                            set_error(d_err, SPARSE_ERR_INTERNAL);
+                            w = 2ull << 62;
+                        }
+                        continue;
+                    }
+                    if (spins > 64) __nanosleep(64);
+                    if ((w >> 62) == 0ull) w = ld_volatile(dstatus + jj);
+                }
+                const uint32_t incl = __ballot_sync(kFull, (w >> 62) == 2ull);
+                if (incl) {
+                    const int first = __ffs(incl) - 1;
+                    excl += warp_sum_u64(lane <= first ? (w & kValMask) : 0ull);
+                    break;
+                }
+                excl += warp_sum_u64(w & kValMask);
+                top -= 32;
+            }
+            if (lane == 0) st_volatile(dstatus + tile, (2ull << 62) | (excl + agg));
+        }
+        if (lane == 0) s_excl = excl;
+    }
+    __syncthreads();
+    const unsigned long long ex = s_excl;
+    uint32_t h_run = static_cast<uint32_t>(ex >> 31) + (xe >> 16);       // heads before p0
+    uint32_t p_run = static_cast<uint32_t>(ex & 0x7fffffffull) + (xe & 0xffffu);
+
+#pragma unroll
+    for (int i = 0; i < kRunItems; ++i) {
+        const uint32_t q = p0 + i;
+        if (q >= n) break;
+        const bool h = (headm >> i) & 1u;
+        if (h) ++h_run;
+        const uint32_t u = h_run - 1;  // segment of position q
+        if (h) {
+            seg_off[u] = q;
+            if (idx_out) idx_out[u] = static_cast<int64_t>(k[i]);
+            if (seg_off_out) seg_off_out[u] = static_cast<int64_t>(q);
+            if (ls && static_cast<int64_t>(k[i]) < bound) {
+                if (!ls_per_coord) {
+                    if (ls[k[i]] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                } else {
+                    const int64_t b = static_cast<int64_t>(k[i]) * c;
+                    for (int64_t jc = 0; jc < c; ++jc)
+                        if (ls[b + jc] >= t) {
+                            set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                            break;
+                        }
+                }
+            }
+        }
+        const uint32_t pm = sperm[q];
+        if (perm_out) perm_out[q] = static_cast<int64_t>(pm);
+        if ((piecem >> i) & 1u) {
+            bool multi = true;
+            if (h) {
+                const uint32_t nxt = (q / kPieceLen + 1) * kPieceLen;
+                multi = (nxt < n) && (skey[nxt] == k[i]);
+            }
+            rec[p_run] = make_uint4(q, k[i], u | (multi ? kMultiFlag : 0u), pm);
+            ++p_run;
+        }
+    }
+    if (tile == gridDim.x - 1 && tid == 0) {
+        const uint32_t U = static_cast<uint32_t>((ex + agg) >> 31);
+        const uint32_t P = static_cast<uint32_t>((ex + agg) & 0x7fffffffull);
+        counts[kCntU] = U;
+        counts[kCntP] = P;
+        seg_off[U] = n;
+        rec[P] = make_uint4(n, 0u, 0u, 0u);
+        if (seg_off_out) seg_off_out[U] = static_cast<int64_t>(n);
+        if (d_nnz_out) *d_nnz_out = static_cast<int64_t>(U);
+    }
+}
+
+cudaError_t sort_and_segment(const int64_t* idx, int64_t n, int64_t c, int64_t bound, const WsLayout& L,
+                             SortWs& ws, int64_t* idx_out, int64_t* seg_off_out, int64_t* perm_out,
+                             int64_t* d_nnz_out, const int64_t* ls, int ls_per_coord, int64_t t,
+                             int32_t* d_err, cudaStream_t s)
+{
+    cudaError_t e;
+    {
+        SO_PROFILE("memset_control", s);
+        e = cudaMemsetAsync(ws.gh, 0, L.ctrl_end - L.ctrl_begin, s);
+    }
+    if (e != cudaSuccess) return e;
+    const uint32_t nn = static_cast<uint32_t>(n);
+    const int hist_blocks =
+        static_cast<int>(std::min<int64_t>((n + kBlock * 16 - 1) / (kBlock * 16), 4 * num_sms()));
+    {
+        SO_PROFILE("range_hist", s);
+        k_range_hist<<<hist_blocks, kBlock, 0, s>>>(idx, nn, bound, L.passes, ws.gh, d_err);
+    }
+    for (int p = 0; p < L.passes; ++p) {
+        const int out = p & 1;
+        const int in = out ^ 1;
+        uint32_t* st = ws.rstatus + static_cast<size_t>(p) * L.sort_tiles * 256;
+        SO_PROFILE("radix_pass", s);
+        if (p == 0)
+            k_radix_pass<true><<<L.sort_tiles, kBlock, 0, s>>>(idx, nullptr, nullptr, ws.keys[out],
+                                                               ws.vals[out], nn, 8 * p, ws.gh + 256 * p, st,
+                                                               ws.counts + kCtrPass0 + p, d_err);
+        else
+            k_radix_pass<false><<<L.sort_tiles, kBlock, 0, s>>>(nullptr, ws.keys[in], ws.vals[in],
+                                                                ws.keys[out], ws.vals[out], nn, 8 * p,
+                                                                ws.gh + 256 * p, st,
+                                                                ws.counts + kCtrPass0 + p, d_err);
+    }
+    SO_PROFILE("run_detect", s);
+    k_run_detect<<<L.run_tiles, kBlock, 0, s>>>(ws.keys[ws.final_buf], ws.vals[ws.final_buf], nn, ws.rec,
+                                                ws.seg_off, ws.dstatus, ws.counts + kCtrRun, ws.counts,
+                                                idx_out, seg_off_out, perm_out, d_nnz_out, ls, ls_per_coord,
+                                                c, bound, t, d_err);
+    return cudaGetLastError();
+}
+
+// Canonical row-COO check: rows strictly ascending in [0, r); last_step < t.
+__global__ void __launch_bounds__(kBlock) k_check_rows(const int64_t* __restrict__ rows, int64_t n,
+                                                       int64_t r, int64_t c, const int64_t* __restrict__ ls,
+                                                       int ls_per_coord, int64_t t, int32_t* d_err)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; i < n; i += stride) {
+        const int64_t k = rows[i];
+        if (k < 0 || k >= r) {
+            set_error(d_err, SPARSE_ERR_INDEX_OUT_OF_RANGE);
+            continue;
+        }
+        if (i > 0 && rows[i - 1] >= k) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
+        if (ls) {
+            if (!ls_per_coord) {
+                if (ls[k] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+            } else {
+                for (int64_t j = 0; j < c; ++j)
+                    if (ls[k * c + j] >= t) {
+                        set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                        break;
+                    }
+            }
+        }
+    }
+}
+
+cudaError_t check_canonical_rows(const int64_t* rows, int64_t n, int64_t r, int64_t c, const int64_t* ls,
+                                 int ls_per_coord, int64_t t, int32_t* d_err, cudaStream_t s)
+{
+    const int blocks = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>((n + kBlock - 1) / kBlock, 8 * num_sms())));
+    SO_PROFILE("check_rows", s);
+    k_check_rows<<<blocks, kBlock, 0, s>>>(rows, n, r, c, ls, ls_per_coord, t, d_err);
+    return cudaGetLastError();
+}
+
+}  // namespace so
