@@ -41,5 +41,7 @@ def cuda_lib():
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    import lazy_optimizers_embedding_gb300 as so
-    return so
+    import __graft_entry__
+    __graft_entry__.build()
+    from lazy_optimizers_embedding_gb300 import binding
+    return binding

@@ -1,0 +1,583 @@
+"""GPU path (through the C-ABI) against the CPU oracle, element by element.
+
+Sizes: the oracle finishes each case in well under a second, while the inputs
+still span several radix / run-detection tiles (2,048 entries each), several
+pieces of 32 sorted entries, a ragged tail, and hot keys with enough duplicates
+to need two levels of the partial-combining tree (> 32*32 entries of one key).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_harness import assert_state_close, dev, host, max_rel, tol_violations
+
+pytestmark = pytest.mark.gpu
+
+ADAM = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8)
+
+
+def _raw_rows(rng, n, bound, hot=None, hot_count=0):
+    idx = rng.integers(0, bound, n).astype(np.int64)
+    if hot is not None and hot_count:
+        pos = rng.choice(n, size=min(hot_count, n), replace=False)
+        idx[pos] = hot
+    return idx
+
+
+# ------------------------------------------------------------------ canonicalize
+CANON_CASES = [
+    # (n, c, bound, hot_count)
+    (1, 1, 1, 0),
+    (7, 3, 10, 0),
+    (2048, 4, 1000, 0),
+    (5000, 1, 10_000_000, 0),
+    (5000, 32, 1000, 1500),
+    (9000, 64, 4000, 3000),
+    (20000, 128, 50_000, 4500),
+    (3001, 256, 50, 0),
+    (1500, 1000, 300, 200),
+    (4096, 5, 1, 0),          # every entry the same key
+    (70_000, 2, 100_000, 0),
+]
+
+
+@pytest.mark.parametrize("n,c,bound,hot", CANON_CASES)
+def test_canonicalize_matches_oracle(cuda_lib, n, c, bound, hot):
+    so = cuda_lib
+    import torch
+    rng = np.random.default_rng(n * 7 + c)
+    idx = _raw_rows(rng, n, bound, hot=bound - 1, hot_count=hot)
+    vals = rng.standard_normal((n, c)).astype(np.float32)
+    vals[rng.integers(0, n, max(1, n // 50))] = -0.0
+    ri, rv, rseg, rperm = oracle.canonicalize(idx, vals, bound)
+    u = ri.shape[0]
+    d_idx = dev(idx)
+    d_vals = dev(vals)
+    idx_out = torch.empty(n, dtype=torch.int64, device="cuda")
+    vals_out = torch.empty((n, c), dtype=torch.float32, device="cuda")
+    seg_out = torch.empty(n + 1, dtype=torch.int64, device="cuda")
+    perm_out = torch.empty(n, dtype=torch.int64, device="cuda")
+    nnz = torch.zeros(1, dtype=torch.int64, device="cuda")
+    ws = so.workspace(n, c, bound)
+    err = so.error_word()
+    so.check(so.sparse_canonicalize(d_idx, d_vals, n, c, bound, idx_out, vals_out, seg_out, perm_out, nnz, ws,
+                                    err), "canonicalize")
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert int(nnz.item()) == u
+    assert np.array_equal(host(idx_out)[:u], ri)
+    assert np.array_equal(host(seg_out)[:u + 1], rseg)
+    assert np.array_equal(host(perm_out), rperm)
+    gv = host(vals_out)[:u].reshape(u, c)
+    rv = rv.reshape(u, c)
+    bad = tol_violations(gv, rv)
+    assert not bad.any(), f"{int(bad.sum())} values outside tolerance, max rel {max_rel(gv, rv)}"
+    single = np.diff(rseg) == 1
+    assert gv[single].tobytes() == rv[single].tobytes(), "a lone value must pass through bit for bit"
+
+
+def test_canonicalize_empty_and_deterministic(cuda_lib):
+    so = cuda_lib
+    import torch
+    err = so.error_word()
+    nnz = torch.full((1,), 7, dtype=torch.int64, device="cuda")
+    seg = torch.full((1,), 7, dtype=torch.int64, device="cuda")
+    e = torch.empty(0, dtype=torch.int64, device="cuda")
+    so.check(so.sparse_canonicalize(e, torch.empty(0, device="cuda"), 0, 4, 10, e, None, seg, None, nnz, None, err))
+    torch.cuda.synchronize()
+    assert int(nnz.item()) == 0 and int(seg.item()) == 0
+    rng = np.random.default_rng(3)
+    n, c, bound = 30000, 64, 2000
+    idx = _raw_rows(rng, n, bound, hot=5, hot_count=9000)
+    vals = rng.standard_normal((n, c)).astype(np.float32)
+    d_idx, d_vals = dev(idx), dev(vals)
+    outs = []
+    for _ in range(2):
+        vo = torch.empty((n, c), device="cuda")
+        io = torch.empty(n, dtype=torch.int64, device="cuda")
+        so.check(so.sparse_canonicalize(d_idx, d_vals, n, c, bound, io, vo, None, None, nnz,
+                                        so.workspace(n, c, bound), err))
+        torch.cuda.synchronize()
+        u = int(nnz.item())
+        outs.append((u, host(io)[:u], host(vo)[:u]))
+    assert int(err.item()) == 0
+    assert outs[0][0] == outs[1][0]
+    assert np.array_equal(outs[0][1], outs[1][1]) and outs[0][2].tobytes() == outs[1][2].tobytes()
+
+
+# ------------------------------------------------------------------ lazy Adam, raw row-COO
+def _run_adam(so, R, c, steps, mode, gen, form, layout=None, hp=ADAM, check_every=False):
+    """gen(step) -> gradient for the step, in the given form; runs GPU and oracle side by side."""
+    import torch
+    rng = np.random.default_rng(R + c)
+    p0 = (rng.standard_normal((R, c)) * 0.01).astype(np.float32)
+    per_coord = layout == so.LAST_STEP_PER_COORD
+    ls_n = R * c if per_coord else R
+    p, m, v = dev(p0), torch.zeros((R, c), device="cuda"), torch.zeros((R, c), device="cuda")
+    ls = torch.zeros(ls_n, dtype=torch.int64, device="cuda")
+    op, om, ov, ols = p0.copy(), np.zeros_like(p0), np.zeros_like(p0), np.zeros(ls_n, np.int64)
+    err = so.error_word()
+    cfg = so.AdamConfig(**hp)
+    omode = oracle.MODE_DORMANCY_DECAY if mode == so.DORMANCY_DECAY else oracle.MODE_LAZY
+    touched = np.zeros((R, c), bool)
+    ws = None
+    for s in range(steps):
+        t = s + 1
+        g = gen(s)
+        if form == "raw" or form == "canon":
+            rows, vals = g
+            if ws is None and form == "raw":
+                ws = so.workspace(max(rows.shape[0], 1), c, R)
+            grad = so.row_coo(dev(rows), dev(vals), form == "canon")
+            so.check(so.sparse_adam_table_step(p, m, v, ls, layout or so.LAST_STEP_PER_ROW, R, c, grad, t, cfg, mode,
+                                               ws, err), "adam_table_step")
+            rc = oracle.adam_table_step(op, om, ov, ols, t, rows=rows, vals=vals, is_canonical=(form == "canon"),
+                                        mode=omode, ls_per_coord=per_coord, **hp)
+            touched[np.unique(rows)] = True
+        else:
+            row_off, cols, vals = g
+            grad = so.csr(dev(row_off), dev(cols), dev(vals))
+            so.check(so.sparse_adam_table_step(p, m, v, ls, layout, R, c, grad, t, cfg, mode, None, err),
+                     "adam_table_step csr")
+            rc = oracle.adam_table_step(op, om, ov, ols, t, row_off=row_off, cols=cols, vals=vals, mode=omode,
+                                        ls_per_coord=per_coord, **hp)
+            rr = np.repeat(np.arange(R), np.diff(row_off))
+            touched[rr, cols] = True
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, so.status_string(int(err.item()))
+        if check_every or s == steps - 1:
+            assert_state_close(f"p@t={t}", host(p), op, touched, p0)
+            assert_state_close(f"m@t={t}", host(m), om)
+            assert_state_close(f"v@t={t}", host(v), ov)
+            assert np.array_equal(host(ls), ols), f"last_step@t={t}"
+    return host(p), host(m), host(v)
+
+
+RAW_CASES = [(1, 1), (3, 3), (2000, 4), (3000, 32), (3000, 64), (2500, 128), (800, 256), (300, 1000)]
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["lazy", "dormancy_decay"])
+@pytest.mark.parametrize("R,c", RAW_CASES)
+def test_adam_raw_rows(cuda_lib, mode, R, c):
+    so = cuda_lib
+
+    def gen(s):
+        rng = np.random.default_rng(1000 + s)
+        n = 4000 if R > 3 else 50
+        rows = _raw_rows(rng, n, R, hot=R // 2, hot_count=(1500 if s % 2 == 0 else 0) if R > 3 else 0)
+        if R > 3:  # dormant rows: touch only part of the table per step
+            rows = rows % max(1, R // (1 + s % 3))
+        return rows, (rng.standard_normal((n, c)) * 0.01).astype(np.float32)
+
+    _run_adam(so, R, c, 5, mode, gen, "raw", check_every=True)
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["lazy", "dormancy_decay"])
+@pytest.mark.parametrize("R,c", [(5000, 1), (4000, 64), (3000, 128), (1000, 12)])
+def test_adam_canonical_rows(cuda_lib, mode, R, c):
+    so = cuda_lib
+
+    def gen(s):
+        rng = np.random.default_rng(2000 + s)
+        rows = np.sort(rng.choice(R, size=R // 3, replace=False)).astype(np.int64)
+        return rows, rng.standard_normal((rows.shape[0], c)).astype(np.float32)
+
+    _run_adam(so, R, c, 4, mode, gen, "canon", check_every=True)
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["lazy", "dormancy_decay"])
+def test_adam_raw_rows_per_coord_last_step(cuda_lib, mode):
+    so = cuda_lib
+
+    def gen(s):
+        rng = np.random.default_rng(3000 + s)
+        rows = _raw_rows(rng, 3000, 900, hot=3, hot_count=1200)
+        return rows, rng.standard_normal((3000, 16)).astype(np.float32)
+
+    _run_adam(so, 900, 16, 4, mode, gen, "raw", layout=so.LAST_STEP_PER_COORD)
+
+
+def _csr_elem(rng, R, c, nrows, k):
+    rows = np.sort(rng.choice(R, size=nrows, replace=False))
+    counts = np.zeros(R, np.int64)
+    counts[rows] = k
+    row_off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    cols = np.sort(np.argsort(rng.random((nrows, c)), axis=1)[:, :k], axis=1).astype(np.int32).reshape(-1)
+    return row_off, cols, rng.standard_normal(cols.shape[0]).astype(np.float32)
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["lazy", "dormancy_decay"])
+@pytest.mark.parametrize("R,c,nrows,k", [(2000, 256, 300, 16), (5000, 7, 1200, 3), (64, 40, 64, 40)])
+def test_adam_csr_element_granular(cuda_lib, mode, R, c, nrows, k):
+    so = cuda_lib
+    _run_adam(so, R, c, 5, mode, lambda s: _csr_elem(np.random.default_rng(4000 + s), R, c, nrows, k), "csr",
+              layout=so.LAST_STEP_PER_COORD, check_every=True)
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["lazy", "dormancy_decay"])
+def test_adam_csr_full_rows_per_row_last_step(cuda_lib, mode):
+    """A CSR whose listed rows are full, with one last_step per row (the summed-lookups shape)."""
+    so = cuda_lib
+    R, c = 3000, 64
+
+    def gen(s):
+        rng = np.random.default_rng(5000 + s)
+        rows = np.sort(rng.choice(R, size=700, replace=False))
+        ro, co = oracle.row_coo_to_csr(rows, R, c)
+        return ro, co, rng.standard_normal(rows.shape[0] * c).astype(np.float32)
+
+    _run_adam(so, R, c, 5, mode, gen, "csr", layout=so.LAST_STEP_PER_ROW, check_every=True)
+
+
+def test_summed_lookups_to_csr_then_step(cuda_lib):
+    """Raw Zipf lookups -> GPU canonicalise -> GPU row-COO to CSR -> GPU CSR step, against the
+    oracle's own canonicalise -> CSR -> step (each side from the same raw lookups)."""
+    so = cuda_lib
+    import torch
+    from lazy_optimizers_embedding_gb300 import workloads as wl
+    w = wl.CFG_ZIPF_1M_64.scaled(rows=20_000, lookups=6000, steps=4)
+    R, c = w.rows, w.cols
+    p0 = wl.table_init(w)
+    p, m, v = dev(p0), torch.zeros((R, c), device="cuda"), torch.zeros((R, c), device="cuda")
+    ls = torch.zeros(R, dtype=torch.int64, device="cuda")
+    op, om, ov, ols = p0.copy(), np.zeros_like(p0), np.zeros_like(p0), np.zeros(R, np.int64)
+    err = so.error_word()
+    cfg = so.AdamConfig(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps)
+    ws = so.workspace(w.lookups, c, R)
+    for s in range(w.steps):
+        t = s + 1
+        idx, vals = wl.coo_step(w, s)
+        n = idx.shape[0]
+        d_idx, d_vals = dev(idx), dev(vals)
+        io = torch.empty(n, dtype=torch.int64, device="cuda")
+        vo = torch.empty((n, c), device="cuda")
+        nnz = torch.zeros(1, dtype=torch.int64, device="cuda")
+        so.check(so.sparse_canonicalize(d_idx, d_vals, n, c, R, io, vo, None, None, nnz, ws, err))
+        torch.cuda.synchronize()
+        u = int(nnz.item())
+        ro = torch.empty(R + 1, dtype=torch.int64, device="cuda")
+        co = torch.empty(max(u * c, 1), dtype=torch.int32, device="cuda")
+        so.check(so.sparse_row_coo_to_csr(io, u, R, c, ro, co, err))
+        vals_csr = vo[:u].contiguous().view(-1)
+        so.check(so.sparse_adam_table_step(p, m, v, ls, so.LAST_STEP_PER_ROW, R, c,
+                                           so.csr(ro, co[:u * c], vals_csr), t, cfg, so.DORMANCY_DECAY, None, err))
+        ci, cv, _, _ = oracle.canonicalize(idx, vals, R)
+        oro, oco = oracle.row_coo_to_csr(ci, R, c)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, so.status_string(int(err.item()))
+        assert np.array_equal(host(ro), oro) and np.array_equal(host(co)[:u * c], oco)
+        assert oracle.adam_table_step(op, om, ov, ols, t, row_off=oro, cols=oco, vals=cv.reshape(-1),
+                                      mode=oracle.MODE_DORMANCY_DECAY, lr=w.lr, beta1=w.beta1, beta2=w.beta2,
+                                      eps=w.eps) == 0
+    assert_state_close("p", host(p), op)
+    assert_state_close("m", host(m), om)
+    assert_state_close("v", host(v), ov)
+    assert np.array_equal(host(ls), ols)
+
+
+# ------------------------------------------------------------------ 1-D
+@pytest.mark.parametrize("mode", [0, 1], ids=["lazy", "dormancy_decay"])
+@pytest.mark.parametrize("canonical", [True, False])
+def test_adam_1d(cuda_lib, mode, canonical):
+    so = cuda_lib
+    import torch
+    from lazy_optimizers_embedding_gb300 import workloads as wl
+    w = wl.CFG_1D
+    dim = w.rows
+    rng = np.random.default_rng(9)
+    p0 = wl.table_init(w).reshape(-1)
+    p, m, v = dev(p0), torch.zeros(dim, device="cuda"), torch.zeros(dim, device="cuda")
+    ls = torch.zeros(dim, dtype=torch.int64, device="cuda")
+    op, om, ov, ols = p0.copy(), np.zeros_like(p0), np.zeros_like(p0), np.zeros(dim, np.int64)
+    err = so.error_word()
+    cfg = so.AdamConfig(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps)
+    omode = oracle.MODE_DORMANCY_DECAY if mode else oracle.MODE_LAZY
+    ws = so.workspace(3000, 1, dim)
+    for s in range(w.steps):
+        t = s + 1
+        if canonical:
+            idx, g = wl.coo_step(w, s)
+            g = g.reshape(-1)
+        else:
+            idx = rng.integers(0, dim, 3000).astype(np.int64)
+            idx[:500] = 17
+            g = rng.standard_normal(3000).astype(np.float32)
+        d_idx, d_g = dev(idx), dev(g)
+        so.check(so.sparse_adam_step(p, m, v, ls, dim, d_idx, d_g, idx.shape[0], int(canonical), t, cfg, mode,
+                                     None if canonical else ws, err))
+        assert oracle.adam_step(op, om, ov, ols, idx, g, t, is_canonical=canonical, mode=omode, lr=w.lr,
+                                beta1=w.beta1, beta2=w.beta2, eps=w.eps) == 0
+        torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_state_close("p", host(p), op)
+    assert_state_close("m", host(m), om)
+    assert_state_close("v", host(v), ov)
+    assert np.array_equal(host(ls), ols)
+
+
+# ------------------------------------------------------------------ lazy SGD
+@pytest.mark.parametrize("R,c,mom,wd", [(20000, 32, 0.9, 1e-4), (5000, 1, 0.9, 0.0), (3000, 128, 0.0, 0.0),
+                                        (4000, 6, 0.5, 0.1)])
+def test_sgd_raw_rows(cuda_lib, R, c, mom, wd):
+    so = cuda_lib
+    import torch
+    rng = np.random.default_rng(R + c)
+    p0 = (rng.standard_normal((R, c)) * 0.01).astype(np.float32)
+    p = dev(p0)
+    buf = torch.zeros_like(p) if mom else None
+    op, ob = p0.copy(), np.zeros_like(p0)
+    err = so.error_word()
+    cfg = so.SgdConfig(lr=0.05, momentum=mom, weight_decay=wd)
+    n = 6000
+    ws = so.workspace(n, c, R)
+    touched = np.zeros(R, bool)
+    for s in range(6):
+        rows = _raw_rows(rng, n, R, hot=R - 1, hot_count=1100 if s == 2 else 0)
+        vals = rng.standard_normal((n, c)).astype(np.float32)
+        so.check(so.sparse_sgd_table_step(p, buf, R, c, so.row_coo(dev(rows), dev(vals), False), cfg, ws, err))
+        assert oracle.sgd_table_step(op, ob if mom else None, rows=rows, vals=vals, lr=0.05, momentum=mom,
+                                     weight_decay=wd) == 0
+        touched[rows] = True
+        torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_state_close("p", host(p), op, np.repeat(touched[:, None], c, 1), p0)
+    if mom:
+        assert_state_close("buf", host(buf), ob)
+
+
+def test_sgd_1d_canonical_and_csr(cuda_lib):
+    so = cuda_lib
+    import torch
+    from lazy_optimizers_embedding_gb300 import workloads as wl
+    w = wl.CFG_1D_SGD
+    p0 = wl.table_init(w).reshape(-1)
+    p, buf = dev(p0), torch.zeros(w.rows, device="cuda")
+    op, ob = p0.copy(), np.zeros_like(p0)
+    err = so.error_word()
+    cfg = so.SgdConfig(lr=w.lr, momentum=w.momentum, weight_decay=w.weight_decay)
+    for s in range(w.steps):
+        idx, g = wl.coo_step(w, s)
+        d_idx, d_g = dev(idx), dev(g.reshape(-1))
+        so.check(so.sparse_sgd_step(p, buf, w.rows, d_idx, d_g, idx.shape[0], 1, cfg, None, err))
+        assert oracle.sgd_step(op, ob, idx, g.reshape(-1), lr=w.lr, momentum=w.momentum,
+                               weight_decay=w.weight_decay) == 0
+        torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_state_close("p", host(p), op)
+    assert_state_close("buf", host(buf), ob)
+    # SparseSgdTable with an element-granular CSR gradient
+    R, c = 3000, 20
+    rng = np.random.default_rng(2)
+    t0 = rng.standard_normal((R, c)).astype(np.float32)
+    tp, tb = dev(t0), torch.zeros((R, c), device="cuda")
+    tq, tbq = t0.copy(), np.zeros_like(t0)
+    for s in range(3):
+        ro, co, va = _csr_elem(rng, R, c, 400, 5)
+        so.check(so.sparse_sgd_table_step(tp, tb, R, c, so.csr(dev(ro), dev(co), dev(va)), cfg, None, err))
+        assert oracle.sgd_table_step(tq, tbq, row_off=ro, cols=co, vals=va, lr=w.lr, momentum=w.momentum,
+                                     weight_decay=w.weight_decay) == 0
+        torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_state_close("p", host(tp), tq)
+    assert_state_close("buf", host(tb), tbq)
+
+
+# ------------------------------------------------------------------ conversions
+@pytest.mark.parametrize("r,c,k", [(0, 3, 0), (1, 1, 1), (50, 7, 100), (10_000, 64, 30_000), (3000, 1, 1500),
+                                   (40, 100_000, 5000)])
+def test_csr_coo_round_trip_matches_oracle(cuda_lib, r, c, k):
+    so = cuda_lib
+    import torch
+    rng = np.random.default_rng(r + c + k)
+    lin = np.sort(rng.choice(r * c, size=k, replace=False)).astype(np.int64) if r else np.zeros(0, np.int64)
+    oro, oco = oracle.coo_to_csr(lin, r, c)
+    err = so.error_word()
+    d_lin = dev(lin)
+    ro = torch.empty(r + 1, dtype=torch.int64, device="cuda")
+    co = torch.empty(max(k, 1), dtype=torch.int32, device="cuda")
+    so.check(so.sparse_coo_to_csr(d_lin, k, r, c, ro, co, err))
+    back = torch.empty(max(k, 1), dtype=torch.int64, device="cuda")
+    so.check(so.sparse_csr_to_coo(ro, co, r, c, k, back, err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(host(ro), oro)
+    assert np.array_equal(host(co)[:k], oco)
+    assert np.array_equal(host(back)[:k], lin)
+
+
+def test_golden_csr_coo_on_gpu(cuda_lib):
+    """The hand-derived CSR <-> COO fixture ("Sparse gradient representations") on the GPU."""
+    so = cuda_lib
+    import torch
+    from conftest import read_cases
+    for case in read_cases("csr_coo_linear_index.txt"):
+        r, c = map(int, case["shape"][0])
+        row_off = np.array(case["row_offsets"][0], np.int64)
+        cols = np.array(case["col_indices"][0], np.int32)
+        lin = np.array(case["linear"][0], np.int64)
+        err = so.error_word()
+        d_ro, d_co, d_lin = dev(row_off), dev(cols), dev(lin)
+        out = torch.empty(lin.shape[0], dtype=torch.int64, device="cuda")
+        so.check(so.sparse_csr_to_coo(d_ro, d_co, r, c, lin.shape[0], out, err))
+        ro = torch.empty(r + 1, dtype=torch.int64, device="cuda")
+        co = torch.empty(lin.shape[0], dtype=torch.int32, device="cuda")
+        so.check(so.sparse_coo_to_csr(d_lin, lin.shape[0], r, c, ro, co, err))
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert np.array_equal(host(out), lin)
+        assert np.array_equal(host(ro), row_off) and np.array_equal(host(co), cols)
+
+
+def test_golden_duplicate_sum_on_gpu(cuda_lib):
+    so = cuda_lib
+    import torch
+    from conftest import read_cases
+    for case in read_cases("duplicate_sum.txt"):
+        bound = int(case["bound"][0][0])
+        c = int(case["cols"][0][0])
+        idx = np.array(case["idx"][0], np.int64)
+        n = idx.shape[0]
+        vals = np.array([float(x) for x in case["vals"][0]], np.float32).reshape(n, c)
+        d_idx, d_vals = dev(idx), dev(vals)
+        io = torch.empty(n, dtype=torch.int64, device="cuda")
+        vo = torch.empty((n, c), device="cuda")
+        so_ = torch.empty(n + 1, dtype=torch.int64, device="cuda")
+        po = torch.empty(n, dtype=torch.int64, device="cuda")
+        nnz = torch.zeros(1, dtype=torch.int64, device="cuda")
+        err = so.error_word()
+        so.check(so.sparse_canonicalize(d_idx, d_vals, n, c, bound, io, vo, so_, po, nnz,
+                                        so.workspace(n, c, bound), err))
+        torch.cuda.synchronize()
+        u = int(nnz.item())
+        assert list(host(io)[:u]) == [int(x) for x in case["canonical_idx"][0]]
+        want = np.array([float(x) for x in case["canonical_vals"][0]], np.float32).reshape(-1, c)
+        assert host(vo)[:u].tobytes() == want.tobytes()
+        assert list(host(so_)[:u + 1]) == [int(x) for x in case["seg_off"][0]]
+        assert list(host(po)) == [int(x) for x in case["perm"][0]]
+
+
+# ------------------------------------------------------------------ errors: all or nothing
+def test_errors_set_d_err_and_write_nothing(cuda_lib):
+    so = cuda_lib
+    import torch
+    R, c = 100, 8
+    rng = np.random.default_rng(4)
+    p0 = rng.standard_normal((R, c)).astype(np.float32)
+    p, m, v = dev(p0), torch.zeros((R, c), device="cuda"), torch.zeros((R, c), device="cuda")
+    ls0 = np.zeros(R, np.int64)
+    ls0[40] = 9
+    ls = dev(ls0)
+    cfg = so.AdamConfig(**ADAM)
+    ws = so.workspace(64, c, R)
+    g2 = dev(np.ones((2, c), np.float32))
+
+    def step(grad, t=5, layout=so.LAST_STEP_PER_ROW, lsv=ls):
+        err = so.error_word()
+        so.check(so.sparse_adam_table_step(p, m, v, lsv, layout, R, c, grad, t, cfg, so.DORMANCY_DECAY, ws, err))
+        torch.cuda.synchronize()
+        return int(err.item())
+
+    cases = [
+        (so.row_coo(dev(np.array([3, R])), g2, False), so.ERR_INDEX_OUT_OF_RANGE),
+        (so.row_coo(dev(np.array([-1, 3])), g2, False), so.ERR_INDEX_OUT_OF_RANGE),
+        (so.row_coo(dev(np.array([3, R + 5])), g2, True), so.ERR_INDEX_OUT_OF_RANGE),
+        (so.row_coo(dev(np.array([7, 7])), g2, True), so.ERR_NOT_CANONICAL),
+        (so.row_coo(dev(np.array([9, 2])), g2, True), so.ERR_NOT_CANONICAL),
+        (so.row_coo(dev(np.array([40, 2])), g2, False), so.ERR_STEP_ORDER),
+        (so.row_coo(dev(np.array([2, 40])), g2, True), so.ERR_STEP_ORDER),
+    ]
+    for grad, want in cases:
+        assert step(grad) == want
+
+    # CSR: partial row under per-row last_step; unordered columns; column out of range; bad offsets
+    def csr_case(row_off, cols):
+        return so.csr(dev(np.array(row_off, np.int64)), dev(np.array(cols, np.int32)),
+                      dev(np.ones(len(cols), np.float32)))
+
+    partial = [0] * (R + 1)
+    for i in range(1, R + 1):
+        partial[i] = 1 if i > 3 else 0
+    assert step(csr_case(partial, [2])) == so.ERR_NOT_CANONICAL
+    lsc = dev(np.zeros(R * c, np.int64))
+    unordered = [0, 0, 0, 0] + [2] * (R - 3)
+    assert step(csr_case(unordered, [5, 1]), layout=so.LAST_STEP_PER_COORD, lsv=lsc) == so.ERR_NOT_CANONICAL
+    assert step(csr_case(partial, [c]), layout=so.LAST_STEP_PER_COORD, lsv=lsc) == so.ERR_INDEX_OUT_OF_RANGE
+    bad_end = list(partial)
+    bad_end[-1] = 5
+    assert step(csr_case(bad_end, [1]), layout=so.LAST_STEP_PER_COORD, lsv=lsc) == so.ERR_NOT_CANONICAL
+    assert np.array_equal(host(p), p0) and not host(m).any() and not host(v).any()
+    assert np.array_equal(host(ls), ls0) and not host(lsc).any()
+    # sticky: a valid step with a set error word writes nothing
+    err = so.error_word()
+    err.fill_(so.ERR_NOT_CANONICAL)
+    so.check(so.sparse_adam_table_step(p, m, v, ls, so.LAST_STEP_PER_ROW, R, c,
+                                       so.row_coo(dev(np.array([1, 2])), g2, True), 11, cfg, so.LAZY, None, err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == so.ERR_NOT_CANONICAL and np.array_equal(host(p), p0)
+    # host-side rejections return before launching
+    e = so.error_word()
+    bad = so.AdamConfig(lr=1e-3, beta1=1.0, beta2=0.999, eps=1e-8)
+    g = so.row_coo(dev(np.array([1])), dev(np.ones((1, c), np.float32)), True)
+    assert so.sparse_adam_table_step(p, m, v, ls, 0, R, c, g, 12, bad, 1, None, e) == so.ERR_INVALID_ARG
+    assert so.sparse_adam_table_step(p, m, v, ls, 0, R, c, g, 0, cfg, 1, None, e) == so.ERR_INVALID_ARG
+    graw = so.row_coo(dev(np.array([1])), dev(np.ones((1, c), np.float32)), False)
+    assert so.sparse_adam_table_step(p, m, v, ls, 0, R, c, graw, 12, cfg, 1, None, e) == so.ERR_WORKSPACE
+
+
+def test_determinism_raw_zipf(cuda_lib):
+    """Every addition has a fixed order: two runs give bitwise equal state."""
+    so = cuda_lib
+    import torch
+    from lazy_optimizers_embedding_gb300 import workloads as wl
+    w = wl.CFG_ZIPF_10M_128.scaled(rows=50_000, lookups=40_000)
+    p0 = wl.table_init(w)
+    res = []
+    for _ in range(2):
+        p = dev(p0)
+        m, v = torch.zeros_like(p), torch.zeros_like(p)
+        ls = torch.zeros(w.rows, dtype=torch.int64, device="cuda")
+        err = so.error_word()
+        ws = so.workspace(w.lookups, w.cols, w.rows)
+        for s in range(3):
+            idx, vals = wl.coo_step(w, s)
+            so.check(so.sparse_adam_table_step(p, m, v, ls, 0, w.rows, w.cols, so.row_coo(dev(idx), dev(vals), False),
+                                               s + 1, so.AdamConfig(**ADAM), so.DORMANCY_DECAY, ws, err))
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        res.append((host(p), host(m), host(v)))
+    for a, b in zip(*res):
+        assert a.tobytes() == b.tobytes()
+
+
+@pytest.mark.parametrize("beta1,gap_steps", [(0.0, 1), (0.9, 1), (0.9, 500), (0.5, 3000)])
+def test_edge_betas_and_long_gaps(cuda_lib, beta1, gap_steps):
+    """beta1 = 0; gap 1 (DormancyDecay == Lazy); long dormancy (beta^gap underflows)."""
+    so = cuda_lib
+    import torch
+    R, c = 64, 4
+    hp = dict(lr=1e-2, beta1=beta1, beta2=0.99, eps=1e-8)
+    rng = np.random.default_rng(11)
+    p0 = rng.standard_normal((R, c)).astype(np.float32)
+    grads = [rng.standard_normal((2, c)).astype(np.float32) for _ in range(3)]
+    outs = {}
+    for mode in (so.LAZY, so.DORMANCY_DECAY):
+        p, m, v = dev(p0), torch.zeros((R, c), device="cuda"), torch.zeros((R, c), device="cuda")
+        ls = torch.zeros(R, dtype=torch.int64, device="cuda")
+        op, om, ov, ols = p0.copy(), np.zeros_like(p0), np.zeros_like(p0), np.zeros(R, np.int64)
+        err = so.error_word()
+        for k, t in enumerate((1, 1 + gap_steps, 2 + gap_steps)):
+            rows = np.array([0, R - 1], np.int64)
+            g = grads[k]
+            so.check(so.sparse_adam_table_step(p, m, v, ls, 0, R, c, so.row_coo(dev(rows), dev(g), True), t,
+                                               so.AdamConfig(**hp), mode, None, err))
+            assert oracle.adam_table_step(op, om, ov, ols, t, rows=rows, vals=g, is_canonical=True,
+                                          mode=oracle.MODE_DORMANCY_DECAY if mode else oracle.MODE_LAZY, **hp) == 0
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_state_close("p", host(p), op)
+        assert_state_close("m", host(m), om)
+        assert_state_close("v", host(v), ov)
+        outs[mode] = host(p)
+    if gap_steps == 1:  # every touch has gap 1: the two modes coincide bit for bit
+        assert outs[so.LAZY].tobytes() == outs[so.DORMANCY_DECAY].tobytes()
