@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Throughput of the sparse / lazy optimizer step on GB300.
+
+Workload: a 10,000,000 x 128 fp32 embedding table (p, m, v: 15.4 GB; last_step
+int64 per row); every step is a raw COO gradient of 262,144 row lookups drawn
+Zipf(1.05) (unsorted, with duplicates), values N(0, 0.01^2).  One step =
+canonicalise (range check, radix sort, run detection, segmented sum of
+duplicates) + lazy Adam (DormancyDecay by default, --mode lazy for Lazy) on the
+touched rows, through the C-ABI entry point sparse_adam_table_step.
+
+Metric: updated coordinates per second (touched rows x 128), whole job.  The
+JSON line also carries the achieved algorithmic HBM bandwidth, a roofline object
+for the dominant kernel (timed live with the library's per-kernel CUDA events on
+the launch stream), an end-to-end number with host<->device copies, and the CPU
+oracle timed on the host cores.
+
+Launch: python bench.py [--gpus 1 --steps K --warmup W]; for N > 1 under
+torchrun, every rank runs an independent replica of the workload on its own GPU
+(no collective on the data path: weak scaling).  --impl reference times the CPU
+oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from lazy_optimizers_embedding_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "sparse Adam step: updated coords/s and achieved HBM GB/s vs ~8 TB/s peak"
+W_CFG = wl.CFG_ZIPF_10M_128
+
+
+# ---------------------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(elapsed_s: float, units: float, world: int, device=None):
+    """Whole-job numbers: max elapsed over ranks, total units over ranks."""
+    if world == 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the GPU is under load."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", f"-lms={interval_ms}"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[1]) for r in rows) if v is not None]
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------- peaks and bytes
+def hbm_peak():
+    try:
+        pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        if pk.get("hbm_gbs"):
+            return float(pk["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except (OSError, ValueError):
+        pass
+    return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def step_bytes(u_rows, c, n, dd):
+    """Algorithmic bytes of one raw row-COO lazy Adam step: touched state rows (p, m, v) read and
+    written, last_step (read in DormancyDecay, written always), gradient values and indices read."""
+    return u_rows * c * 4 * 3 * 2 + u_rows * 8 * (2 if dd else 1) + n * c * 4 + n * 8
+
+
+def fused_kernel_bytes(u_rows, c, n, dd):
+    """Bytes the row-fused update kernel moves by definition: state rows, last_step, gradient values."""
+    return u_rows * c * 4 * 3 * 2 + u_rows * 8 * (2 if dd else 1) + n * c * 4
+
+
+def host_inputs(n_batches, threads):
+    batches = wl.coo_steps_parallel(W_CFG, range(n_batches), threads=threads)
+    u_rows = [int(np.unique(idx).shape[0]) for idx, _ in batches]
+    return batches, u_rows
+
+
+def oracle_steps(p, m, v, ls, batches, u_rows, first_t, steps, dd, budget_s=None):
+    """Runs the CPU oracle over `steps` steps; returns (updated coords, seconds spent in the oracle)."""
+    import oracle
+    w = W_CFG
+    mode = oracle.MODE_DORMANCY_DECAY if dd else oracle.MODE_LAZY
+    spent, units, done = 0.0, 0, 0
+    for k in range(steps):
+        b = (first_t - 1 + k) % len(batches)
+        idx, vals = batches[b]
+        t0 = time.perf_counter()
+        rc = oracle.adam_table_step(p, m, v, ls, first_t + k, rows=idx, vals=vals, mode=mode, lr=w.lr,
+                                    beta1=w.beta1, beta2=w.beta2, eps=w.eps)
+        spent += time.perf_counter() - t0
+        assert rc == 0, rc
+        units += u_rows[b] * w.cols
+        done += 1
+        if budget_s is not None and spent >= budget_s:
+            break
+    return units, spent, done
+
+
+def config_dict(dd, n_batches, world):
+    w = W_CFG
+    return {"workload": f"table {w.rows:,} x {w.cols} fp32, raw COO {w.lookups:,} lookups/step Zipf({w.zipf_s}) "
+                        f"with duplicates, canonicalise + lazy Adam ({'DormancyDecay' if dd else 'Lazy'})",
+            "rows": w.rows, "cols": w.cols, "lookups_per_step": w.lookups, "zipf_s": w.zipf_s,
+            "mode": "dormancy_decay" if dd else "lazy", "last_step": "int64 per row",
+            "lr": w.lr, "beta1": w.beta1, "beta2": w.beta2, "eps": w.eps,
+            "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2: each step reads a fresh 134 MB gradient batch and ~260 MB of touched "
+                  "state (L2 is 129 MB); Zipf-hot rows may stay L2-resident across steps",
+            "distinct_batches": n_batches}
+
+
+# ---------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from lazy_optimizers_embedding_gb300 import binding as so
+    K, W = args.steps, args.warmup
+    dd = args.mode == "dd"
+    w = W_CFG
+    threads = os.cpu_count() or 8
+    n_batches = min(K + W, args.distinct)
+    batches, u_rows = host_inputs(n_batches, threads)
+    p0 = wl.table_init(w, threads=threads)
+
+    p = torch.from_numpy(p0).to(device)
+    m = torch.zeros_like(p)
+    v = torch.zeros_like(p)
+    ls = torch.zeros(w.rows, dtype=torch.int64, device=device)
+    d_in = [(torch.from_numpy(i).to(device), torch.from_numpy(x).to(device)) for i, x in batches]
+    grads = [so.row_coo(i, x, False) for i, x in d_in]
+    ws = so.workspace(w.lookups, w.cols, w.rows, device)
+    err = so.error_word(device)
+    cfg = so.AdamConfig(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps)
+    mode = so.DORMANCY_DECAY if dd else so.LAZY
+    stream = torch.cuda.current_stream(device)
+    state = {"t": 0}
+
+    def step(b, grad=None, s=None):
+        state["t"] += 1
+        rc = so.sparse_adam_table_step(p, m, v, ls, so.LAST_STEP_PER_ROW, w.rows, w.cols,
+                                       grad if grad is not None else grads[b], state["t"], cfg, mode, ws, err,
+                                       s if s is not None else stream)
+        if rc:
+            raise RuntimeError(so.status_string(rc))
+
+    def check_err():
+        e = int(err.item())
+        if e:
+            raise RuntimeError(f"device error word {e}: {so.status_string(e)}")
+
+    batch_of = [i % n_batches for i in range(W + K)]
+    for i in range(W):
+        step(batch_of[i])
+    torch.cuda.synchronize()
+    check_err()
+
+    # ---- device-resident timed region
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.2)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(W, W + K):
+        step(batch_of[i])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    # the same step loop keeps running ~1 s so the clock sampler sees this load
+    t_busy, j = time.time(), 0
+    while time.time() - t_busy < 1.0:
+        for _ in range(20):
+            step(j % n_batches)
+            j += 1
+        torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    check_err()
+    timed = batch_of[W:W + K]
+    units_local = float(sum(u_rows[b] * w.cols for b in timed))
+    bytes_local = float(sum(step_bytes(u_rows[b], w.cols, w.lookups, dd) for b in timed))
+    elapsed_max, units_all = aggregate(elapsed, units_local, world, device)
+
+    # ---- per-kernel times of the same step loop (library CUDA events on the launch stream)
+    so.sparse_profile_reset()
+    so.sparse_profile_enable(True)
+    for b in timed:
+        step(b)
+    torch.cuda.synchronize()
+    prof = so.sparse_profile_read()
+    so.sparse_profile_enable(False)
+    total_prof = sum(ms for _, ms in prof.values())
+    dom = "fused_rows_adam"
+    dom_launches, dom_ms = prof.get(dom, (0, 0.0))
+    dom_bytes = sum(fused_kernel_bytes(u_rows[b], w.cols, w.lookups, dd) for b in timed) / K
+    peak, peak_src = hbm_peak()
+    dom_avg_s = (dom_ms / 1e3) / max(1, dom_launches)
+    achieved = dom_bytes / dom_avg_s / 1e9 if dom_avg_s > 0 else None
+    our_kernels = sum(l for k, (l, _) in prof.items() if k != "memset_control")
+    check_err()
+
+    # ---- end to end: each step's inputs copied from pinned host memory (copy stream,
+    # double-buffered), the C-ABI step, the error word read back to pinned host memory
+    h_in = [(torch.from_numpy(i).pin_memory(), torch.from_numpy(x).pin_memory()) for i, x in batches]
+    stage = [(torch.empty_like(d_in[0][0]), torch.empty_like(d_in[0][1])) for _ in range(2)]
+    stage_grads = [so.row_coo(i, x, False) for i, x in stage]
+    h_err = torch.zeros(1, dtype=torch.int32).pin_memory()
+    copy_stream = torch.cuda.Stream(device)
+    free_ev = [torch.cuda.Event() for _ in range(2)]
+    ready_ev = [torch.cuda.Event() for _ in range(2)]
+    for e in free_ev:
+        e.record(stream)
+
+    def e2e_step(b, slot):
+        hi, hv = h_in[b]
+        di, dv = stage[slot]
+        copy_stream.wait_event(free_ev[slot])
+        with torch.cuda.stream(copy_stream):
+            di.copy_(hi, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+        ready_ev[slot].record(copy_stream)
+        stream.wait_event(ready_ev[slot])
+        step(b, stage_grads[slot])
+        free_ev[slot].record(stream)
+        h_err.copy_(err, non_blocking=True)
+
+    for i in range(2):
+        e2e_step(batch_of[i], i % 2)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    copy_stream.wait_event(e0)
+    for k, i in enumerate(range(W, W + K)):
+        e2e_step(batch_of[i], k % 2)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_elapsed, e2e_units = aggregate(e0.elapsed_time(e1) / 1e3, units_local, world, device)
+    check_err()
+    assert int(h_err.item()) == 0
+    bi = w.lookups * 8 + w.lookups * w.cols * 4
+    bo = 4
+
+    # ---- the oracle on the host cores, bounded sample of the same workload
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        hp = p0  # the device holds its own copy
+        hm, hv = np.zeros_like(hp), np.zeros_like(hp)
+        hls = np.zeros(w.rows, np.int64)
+        units, spent, done = oracle_steps(hp, hm, hv, hls, batches, u_rows, 1, K + W, dd, args.cpu_seconds)
+        cpu = {"value": units / spent, "unit": "coords/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {done} steps of the same workload (full-size table, same seeded inputs); "
+                         f"{spent:.1f} s of single-threaded oracle time (canonicalise + update in fp64)"}
+
+    if rank == 0:
+        achieved_gbs = bytes_local * world / elapsed_max / 1e9
+        line = {
+            "metric": METRIC,
+            "value": units_all / elapsed_max,
+            "unit": "coords/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": W,
+            "ms_per_step": elapsed_max / K * 1e3,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded numpy PCG64: Zipf row indices, normal values; random-init table)",
+            "config": config_dict(dd, n_batches, world),
+            "achieved_hbm_gbs": achieved_gbs,
+            "hbm_frac_of_peak": achieved_gbs / peak,
+            "algorithmic_bytes_per_step": bytes_local / K,
+            "updated_coords_per_step": units_local / K,
+            "gpu_launches": int(our_kernels),
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "peak_source": peak_src, "bytes_per_launch": dom_bytes,
+                         "avg_launch_us": dom_avg_s * 1e6},
+            "kernel_share": {k: {"launches": l, "ms": ms, "share": ms / total_prof if total_prof else None}
+                             for k, (l, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1])},
+            "clocks": dict(clocks or {}, window="timed region plus 1 s of the same step loop"),
+            "e2e": {"value": e2e_units / e2e_elapsed, "unit": "coords/s", "h2d_bytes_per_step": bi,
+                    "d2h_bytes_per_step": bo},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle as the reference arm: same workload, metric and unit (rank 0 only)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    K, W = args.steps, args.warmup
+    dd = args.mode == "dd"
+    w = W_CFG
+    threads = os.cpu_count() or 8
+    n_batches = min(K + W, args.distinct)
+    batches, u_rows = host_inputs(n_batches, threads)
+    p = wl.table_init(w, threads=threads)
+    m, v = np.zeros_like(p), np.zeros_like(p)
+    ls = np.zeros(w.rows, np.int64)
+    oracle_steps(p, m, v, ls, batches, u_rows, 1, W, dd)
+    t0 = time.perf_counter()
+    units, _, _ = oracle_steps(p, m, v, ls, batches, u_rows, W + 1, K, dd)
+    el = time.perf_counter() - t0
+    val = units / el
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "coords/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy PCG64: Zipf row indices, normal values; random-init table)",
+            "config": dict(config_dict(dd, n_batches, 1), parallelism="host CPU oracle, 1 thread"),
+            "cpu_baseline": {"value": val, "unit": "coords/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{K} timed steps after {W} warm-up steps of the full workload"},
+            "e2e": {"value": val, "unit": "coords/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", choices=["dd", "lazy"], default="dd")
+    ap.add_argument("--distinct", type=int, default=64, help="at most this many distinct input batches")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

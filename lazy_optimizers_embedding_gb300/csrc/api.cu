@@ -62,10 +62,12 @@ SgdParams sgd_params(float* p, float* buf, const sparse_sgd_config_t& cfg)
 {
     SgdParams P{};
     P.p = p;
-    P.buf = buf;
+    P.buf = cfg.momentum != 0.0 ? buf : nullptr;  // without momentum the buffer is neither read nor written
     P.lr = static_cast<float>(cfg.lr);
     P.momentum = static_cast<float>(cfg.momentum);
+    P.momentum_lo = static_cast<float>(cfg.momentum - static_cast<double>(P.momentum));
     P.wd = static_cast<float>(cfg.weight_decay);
+    P.wd_lo = static_cast<float>(cfg.weight_decay - static_cast<double>(P.wd));
     return P;
 }
 

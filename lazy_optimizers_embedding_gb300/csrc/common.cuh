@@ -183,7 +183,9 @@ struct AdamParams {
 struct SgdParams {
     float* p;
     float* buf;
-    float lr, momentum, wd;
+    float lr;
+    float momentum, momentum_lo;  // momentum = momentum + momentum_lo (double split into two floats)
+    float wd, wd_lo;              // weight decay, split the same way
 };
 
 struct StoreParams {

@@ -152,10 +152,10 @@ struct CsrSgdOp {
     {
         const int64_t i = row * c + col;
         float p = P.p[i];
-        float b = (P.momentum != 0.0f) ? P.buf[i] : 0.0f;
+        float b = P.buf ? P.buf[i] : 0.0f;
         sgd_coord(P, g, p, b);
         P.p[i] = p;
-        if (P.momentum != 0.0f) P.buf[i] = b;
+        if (P.buf) P.buf[i] = b;
     }
     __device__ __forceinline__ void row_done(int64_t) const {}
 };

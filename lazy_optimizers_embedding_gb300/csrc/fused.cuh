@@ -189,14 +189,25 @@ __device__ __forceinline__ void adam_coord(const AdamParams& P, float b1, float 
 }
 
 // g' = g + wd*p ; buf = mu*buf + g' ; p -= lr*buf   (momentum 0: p -= lr*g').
-// With momentum, mu*buf + g is formed in one fused multiply-add before wd*p is
-// added: mu*buf and g often nearly cancel, and rounding g + wd*p first (at the
-// magnitude of g) would cost the small result its relative accuracy.
+// The momentum buffer is a recursion whose terms mu*buf and g often nearly
+// cancel, so its new value is evaluated error-free and rounded once: mu and wd
+// arrive as hi + lo float pairs (the double hyperparameters to ~2^-48), each
+// product is split exactly with an FMA (TwoProduct), the three terms are added
+// with TwoSum, and the accumulated low parts are added last.  The parameter
+// update uses the unrounded buffer value (hi + tail).
 __device__ __forceinline__ void sgd_coord(const SgdParams& P, float g, float& p, float& b)
 {
-    if (P.momentum != 0.0f) {
-        b = __fmaf_rn(P.wd, p, __fmaf_rn(P.momentum, b, g));
-        p = __fmaf_rn(-P.lr, b, p);
+    if (P.momentum != 0.0f || P.momentum_lo != 0.0f) {
+        const float mh = __fmul_rn(P.momentum, b);
+        const float ml = __fmaf_rn(P.momentum_lo, b, __fmaf_rn(P.momentum, b, -mh));
+        const float wh = __fmul_rn(P.wd, p);
+        const float wl = __fmaf_rn(P.wd_lo, p, __fmaf_rn(P.wd, p, -wh));
+        float s = mh, e = ml;
+        two_sum_acc(s, e, g);
+        two_sum_acc(s, e, wh);
+        const float tail = __fadd_rn(e, wl);
+        b = __fadd_rn(s, tail);
+        p = __fmaf_rn(-P.lr, tail, __fmaf_rn(-P.lr, s, p));
     } else {
         p = __fmaf_rn(-P.lr, __fmaf_rn(P.wd, p, g), p);
     }
@@ -277,7 +288,7 @@ struct SgdEpi {
     {
         const int64_t off = r.key * c + col;
         ld_state<V>(P.p + off, s.p);
-        if (P.momentum != 0.0f) ld_state<V>(P.buf + off, s.b);
+        if (P.buf) ld_state<V>(P.buf + off, s.b);
     }
     template <int V>
     __device__ __forceinline__ void apply(const Row& r, int64_t col, State<V>& s, const float (&g)[V]) const
@@ -286,7 +297,7 @@ struct SgdEpi {
 #pragma unroll
         for (int i = 0; i < V; ++i) sgd_coord(P, g[i], s.p[i], s.b[i]);
         st_state<V>(P.p + off, s.p);
-        if (P.momentum != 0.0f) st_state<V>(P.buf + off, s.b);
+        if (P.buf) st_state<V>(P.buf + off, s.b);
     }
     __device__ __forceinline__ void end_row(const Row&, int, unsigned) const {}
 };
