@@ -38,7 +38,7 @@ sys.path.insert(0, ROOT)
 from lazy_optimizers_embedding_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "sparse Adam step: updated coords/s and achieved HBM GB/s vs ~8 TB/s peak"
-W_CFG = wl.CFG_ZIPF_10M_128
+W_CFG = wl.CFG_ZIPF_10M_128  # replaced by a smaller table with --rows (profiling captures only)
 
 
 # ---------------------------------------------------------------------------- distributed plumbing
@@ -406,7 +406,11 @@ def main(argv=None):
     ap.add_argument("--distinct", type=int, default=64, help="at most this many distinct input batches")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="table rows (default 10,000,000); smaller tables are for ncu captures, not bench lines")
     args = ap.parse_args(argv)
+    if args.rows is not None and args.rows != W_CFG.rows:
+        globals()["W_CFG"] = W_CFG.scaled(name=f"{W_CFG.name}_rows{args.rows}", rows=args.rows)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
