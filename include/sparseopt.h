@@ -219,6 +219,35 @@ sparse_status_t sparse_sgd_table_step(float* p, float* buf, int64_t r, int64_t c
                                       size_t ws_bytes, int32_t* d_err, cudaStream_t stream);
 
 /*
+ * sparse_canonicalize_static_ws -- sparse_canonicalize without a caller workspace
+ * (no counterpart on the pages: this serves callers, not the method).
+ *
+ * For callers that cannot allocate device memory -- code running inside a host
+ * application that owns every device allocation through its own pool, or on a
+ * thread or in a runtime where cudaMalloc is not allowed -- the scratch comes
+ * from one fixed device array of SPARSE_STATIC_WS_BYTES compiled into the
+ * library.  Every GPU that loads the library holds that array until the process
+ * exits.  The call allocates nothing (no cudaMalloc, no cudaFree).
+ *   Arguments, outputs, results and errors are those of sparse_canonicalize,
+ *   without ws / ws_bytes.  Inputs and outputs are still caller memory.
+ *   Limit: the call needs sparse_workspace_size(n, c, bound) <= SPARSE_STATIC_WS_BYTES
+ *   (for example n <= 65,536 entries with c <= 256 columns); larger calls return
+ *   SPARSE_ERR_WORKSPACE before anything is enqueued.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the previous call's
+ *   contents (each call clears what it needs cleared).  Calls whose work
+ *   overlaps on the GPU -- on different streams, or from different host threads
+ *   -- race on the array and give undefined results: serialise them.
+ */
+#define SPARSE_STATIC_WS_BYTES (16u * 1024u * 1024u)
+sparse_status_t sparse_canonicalize_static_ws(const int64_t* idx, const float* vals, int64_t n, int64_t c,
+                                              int64_t bound, int64_t* idx_out, float* vals_out,
+                                              int64_t* seg_off_out, int64_t* perm_out, int64_t* d_nnz_out,
+                                              int32_t* d_err, cudaStream_t stream);
+
+/*
  * Per-kernel timing (diagnostics; no counterpart on the pages).  While enabled,
  * every kernel the library enqueues is bracketed by two CUDA events on its
  * stream.  sparse_profile_read() waits for every recorded event, then reports

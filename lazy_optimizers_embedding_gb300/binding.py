@@ -74,6 +74,7 @@ def _load():
                                          INT, P, SZ, P, P]),
         "sparse_sgd_step": (INT, [P, P, I64, P, P, I64, INT, SgdConfig, P, SZ, P, P]),
         "sparse_sgd_table_step": (INT, [P, P, I64, I64, ctypes.POINTER(Grad), SgdConfig, P, SZ, P, P]),
+        "sparse_canonicalize_static_ws": (INT, [P, P, I64, I64, I64, P, P, P, P, P, P, P]),
         "sparse_profile_enable": (None, [INT]),
         "sparse_profile_reset": (None, []),
         "sparse_profile_read": (INT, [INT, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_int64),
@@ -89,8 +90,9 @@ def _load():
 LIB = _load()
 EXPORTED = ("sparse_workspace_size", "sparse_status_string", "sparse_canonicalize", "sparse_csr_to_coo",
             "sparse_coo_to_csr", "sparse_row_coo_to_csr", "sparse_adam_step", "sparse_adam_table_step",
-            "sparse_sgd_step", "sparse_sgd_table_step", "sparse_profile_enable", "sparse_profile_reset",
-            "sparse_profile_read")
+            "sparse_sgd_step", "sparse_sgd_table_step", "sparse_canonicalize_static_ws", "sparse_profile_enable",
+            "sparse_profile_reset", "sparse_profile_read")
+STATIC_WS_BYTES = 16 * 1024 * 1024  # SPARSE_STATIC_WS_BYTES
 
 
 # ------------------------------------------------------------------ marshalling
@@ -183,6 +185,20 @@ def sparse_canonicalize(idx, vals, n, c, bound, idx_out, vals_out, seg_off_out, 
                                    _ptr(seg_off_out, torch.int64, "seg_off_out"),
                                    _ptr(perm_out, torch.int64, "perm_out"), _ptr(nnz_out, torch.int64, "nnz_out"),
                                    wp, wb, _ptr(d_err, torch.int32, "d_err"), _stream(stream))
+
+
+def sparse_canonicalize_static_ws(idx, vals, n, c, bound, idx_out, vals_out, seg_off_out, perm_out, nnz_out, d_err,
+                                  stream=None) -> int:
+    """sparse_canonicalize with the library's fixed device scratch array instead of a workspace:
+    for callers that cannot allocate device memory (see include/sparseopt.h for the size limit and
+    the rule that calls must not overlap on the GPU)."""
+    return LIB.sparse_canonicalize_static_ws(_ptr(idx, torch.int64, "idx"), _ptr(vals, torch.float32, "vals"),
+                                             int(n), int(c), int(bound), _ptr(idx_out, torch.int64, "idx_out"),
+                                             _ptr(vals_out, torch.float32, "vals_out"),
+                                             _ptr(seg_off_out, torch.int64, "seg_off_out"),
+                                             _ptr(perm_out, torch.int64, "perm_out"),
+                                             _ptr(nnz_out, torch.int64, "nnz_out"), _ptr(d_err, torch.int32, "d_err"),
+                                             _stream(stream))
 
 
 def sparse_csr_to_coo(row_off, cols, r, c, nnz, lin_out, d_err, stream=None) -> int:
