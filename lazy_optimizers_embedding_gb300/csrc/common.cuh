@@ -118,13 +118,14 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* tmp, u
 struct WsLayout {
     int64_t n, c, nb;
     int passes, sort_tiles, run_tiles, levels;
-    size_t keys0, keys1, vals0, vals1, rec, seg_off, part;
+    size_t keys0, keys1, vals0, vals1, rec, seg_off, mlist, part;
     size_t ctrl_begin, gh, counts, rstatus, dstatus, lvl_cnt, ctrl_end;
     size_t total;
 };
 
 // counts[] word indices
-enum { kCtrHist = 0, kCtrPass0 = 1, kCtrRun = 5, kCntU = 8, kCntP = 9, kCountsWords = 16 };
+enum { kCtrHist = 0, kCtrPass0 = 1, kCtrRun = 5, kCntU = 8, kCntP = 9, kCntM = 10, kTicketM = 11, kTicketS = 12,
+       kCountsWords = 16 };
 
 WsLayout ws_layout(int64_t n, int64_t c, int64_t bound);
 
@@ -134,9 +135,10 @@ struct SortWs {
     uint32_t* vals[2];
     uint4* rec;           // [P+1] piece records {start, key, u | multi, perm of start}
     uint32_t* seg_off;    // [U+1]
+    uint32_t* mlist;      // [M] indices of the pieces of multi-piece segments (any order)
     float* part;          // partial sums: [2*nb slots][2][c]
     uint32_t* gh;         // [4][256] digit histograms
-    uint32_t* counts;     // [16]
+    uint32_t* counts;     // [16]: tile counters, U, P, M, work tickets of the fused kernel
     uint32_t* rstatus;    // [passes][sort_tiles][256]
     unsigned long long* dstatus;  // [run_tiles]
     uint32_t* lvl_cnt;    // [levels][2*nb]

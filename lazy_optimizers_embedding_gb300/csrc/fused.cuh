@@ -5,10 +5,11 @@
 // every array is 16-byte aligned), columns col0 + (k*T + tl)*V, k < NV.  A row
 // wider than T*NV*V columns is walked in chunks.
 //
-// Work items are "pieces": runs of at most kPieceLen sorted entries of one
-// segment (one unique index).  A piece whose segment is entirely inside it is
-// summed and applied directly: the team loads the row's optimizer state and the
-// piece's gradient rows together, sums the gradient with error-free TwoSum
+// Work items are "pieces": runs of fewer than 2*kPieceLen sorted entries of one
+// segment (one unique index); a segment of at most kPieceLen entries is always
+// a single piece.  A piece whose segment is entirely inside it is summed and
+// applied directly: the team loads the row's optimizer state and the piece's
+// gradient rows together, sums the gradient with error-free TwoSum
 // compensation, updates and stores.  A segment that spans several pieces (a
 // heavy Zipf head) is reduced by a deterministic tree: every piece writes a
 // compensated partial (sum, error) to a slot, and the last of each group of
@@ -30,17 +31,23 @@
 
 namespace so {
 
-// Blocks of kBlock threads per SM the fused kernel is compiled for (3: at most
-// 80 registers, 24 warps per SM) and gradient rows each lane keeps in flight
-// while summing a piece.  Overridable at build time for tuning sweeps.
+// Blocks of kBlock threads per SM the fused kernel is compiled for (4: at most
+// 64 registers, 32 warps per SM), gradient rows a lane requests at once when a
+// piece holds several entries (kRowIlp; twice that for pieces of split
+// segments), and single pieces a team takes per work ticket.  Overridable at
+// build time for tuning sweeps.
 #ifndef SO_FUSED_MIN_BLOCKS
-#define SO_FUSED_MIN_BLOCKS 3
+#define SO_FUSED_MIN_BLOCKS 4
 #endif
-#ifndef SO_GRAD_BATCH
-#define SO_GRAD_BATCH 2
+#ifndef SO_ROW_ILP
+#define SO_ROW_ILP 4
+#endif
+#ifndef SO_TICKET_CHUNK
+#define SO_TICKET_CHUNK 4
 #endif
 constexpr int kFusedMinBlocks = SO_FUSED_MIN_BLOCKS;
-constexpr int kGradBatch = SO_GRAD_BATCH;
+constexpr int kRowIlp = SO_ROW_ILP;
+constexpr int kTicketChunk = SO_TICKET_CHUNK;
 
 struct PieceInfo {
     int64_t start, end;   // sorted positions [start, end)
@@ -55,8 +62,13 @@ struct SortedSrc {
     const uint4* rec;
     const uint32_t* sperm;
     const uint32_t* seg_off;
+    const uint32_t* mlist;
     const uint32_t* counts;
     __device__ __forceinline__ int64_t count() const { return counts[kCntP]; }
+    __device__ __forceinline__ int64_t count_multi() const { return counts[kCntM]; }
+    __device__ __forceinline__ int64_t multi_index(int64_t t) const { return mlist[t]; }
+    static constexpr bool kTickets = true;
+    __device__ __forceinline__ uint32_t* ticket(int which) const { return const_cast<uint32_t*>(counts) + which; }
     __device__ __forceinline__ PieceInfo piece(int64_t j) const
     {
         const uint4 r = rec[j];
@@ -71,6 +83,7 @@ struct SortedSrc {
         return p;
     }
     __device__ __forceinline__ uint32_t perm(int64_t e) const { return sperm[e]; }
+    __device__ __forceinline__ const uint32_t* perm_ptr(int64_t e) const { return sperm + e; }
     __device__ __forceinline__ void seg_bounds(uint32_t u, int64_t& s0, int64_t& s1) const
     {
         s0 = seg_off[u];
@@ -83,6 +96,10 @@ struct CanonSrc {
     const int64_t* rows;
     int64_t n;
     __device__ __forceinline__ int64_t count() const { return n; }
+    __device__ __forceinline__ int64_t count_multi() const { return 0; }
+    __device__ __forceinline__ int64_t multi_index(int64_t) const { return 0; }
+    static constexpr bool kTickets = false;
+    __device__ __forceinline__ uint32_t* ticket(int) const { return nullptr; }
     __device__ __forceinline__ PieceInfo piece(int64_t j) const
     {
         PieceInfo p;
@@ -95,6 +112,7 @@ struct CanonSrc {
         return p;
     }
     __device__ __forceinline__ uint32_t perm(int64_t e) const { return static_cast<uint32_t>(e); }
+    __device__ __forceinline__ const uint32_t* perm_ptr(int64_t) const { return nullptr; }   // never called: one entry per piece
     __device__ __forceinline__ void seg_bounds(uint32_t, int64_t& s0, int64_t& s1) const { s0 = s1 = 0; }
 };
 
@@ -214,48 +232,42 @@ __device__ __forceinline__ void sgd_coord(const SgdParams& P, float g, float& p,
 }
 
 // ------------------------------------------------------------ epilogues
+// An epilogue owns the optimizer state of a row: kArrays fp32 arrays of r*c
+// values (arrays() of them live), read at the row's columns, updated from the
+// summed gradient and written back; optionally one int64 per row (last_step)
+// read before the update (stage_last) and rewritten after it (end_row).
 struct AdamEpi {
     static constexpr const char* kName = "fused_rows_adam";
+    static constexpr int kArrays = 3;   // p, m, v
     AdamParams P;
     int64_t c;
     struct Row {
         int64_t key;
-        float b1, b2;
+        int64_t last;   // last_step of the row (per-row layout, DormancyDecay)
     };
-    template <int V>
-    struct State {
-        float p[V], m[V], v[V];
-    };
-    __device__ __forceinline__ Row begin_row(const PieceInfo& pc) const
+    __device__ __forceinline__ const int64_t* stage_last(const PieceInfo& pc) const
     {
-        Row r;
-        r.key = pc.key;
-        r.b1 = P.beta1;
-        r.b2 = P.beta2;
-        if (P.dd && !P.ls_per_coord) dormancy_factors(P, P.t - P.ls[pc.key], r.b1, r.b2);
-        return r;
+        return (P.dd && !P.ls_per_coord) ? P.ls + pc.key : nullptr;
     }
+    __device__ __forceinline__ Row make_row(const PieceInfo& pc, int64_t last) const { return Row{pc.key, last}; }
+    __device__ __forceinline__ int arrays() const { return 3; }
+    __device__ __forceinline__ float* array(int a) const { return a == 0 ? P.p : (a == 1 ? P.m : P.v); }
+    __device__ __forceinline__ int64_t base(const PieceInfo& pc) const { return pc.key * c; }
     template <int V>
-    __device__ __forceinline__ void load(const Row& r, int64_t col, State<V>& s) const
+    __device__ __forceinline__ void apply(const Row& r, int64_t col, float (&x)[kArrays][V], const float (&g)[V]) const
     {
         const int64_t off = r.key * c + col;
-        ld_state<V>(P.p + off, s.p);
-        ld_state<V>(P.m + off, s.m);
-        ld_state<V>(P.v + off, s.v);
-    }
-    template <int V>
-    __device__ __forceinline__ void apply(const Row& r, int64_t col, State<V>& s, const float (&g)[V]) const
-    {
-        const int64_t off = r.key * c + col;
+        float rb1 = P.beta1, rb2 = P.beta2;
+        if (P.dd && !P.ls_per_coord) dormancy_factors(P, P.t - r.last, rb1, rb2);
 #pragma unroll
         for (int i = 0; i < V; ++i) {
-            float b1 = r.b1, b2 = r.b2;
+            float b1 = rb1, b2 = rb2;
             if (P.dd && P.ls_per_coord) dormancy_factors(P, P.t - P.ls[off + i], b1, b2);
-            adam_coord(P, b1, b2, g[i], s.p[i], s.m[i], s.v[i]);
+            adam_coord(P, b1, b2, g[i], x[0][i], x[1][i], x[2][i]);
         }
-        st_state<V>(P.p + off, s.p);
-        st_state<V>(P.m + off, s.m);
-        st_state<V>(P.v + off, s.v);
+        st_state<V>(P.p + off, x[0]);
+        st_state<V>(P.m + off, x[1]);
+        st_state<V>(P.v + off, x[2]);
         if (P.ls_per_coord) {
 #pragma unroll
             for (int i = 0; i < V; ++i) P.ls[off + i] = P.t;
@@ -273,31 +285,25 @@ struct AdamEpi {
 
 struct SgdEpi {
     static constexpr const char* kName = "fused_rows_sgd";
+    static constexpr int kArrays = 2;   // p, momentum buffer (absent without momentum)
     SgdParams P;
     int64_t c;
     struct Row {
         int64_t key;
     };
+    __device__ __forceinline__ const int64_t* stage_last(const PieceInfo&) const { return nullptr; }
+    __device__ __forceinline__ Row make_row(const PieceInfo& pc, int64_t) const { return Row{pc.key}; }
+    __device__ __forceinline__ int arrays() const { return P.buf ? 2 : 1; }
+    __device__ __forceinline__ float* array(int a) const { return a == 0 ? P.p : P.buf; }
+    __device__ __forceinline__ int64_t base(const PieceInfo& pc) const { return pc.key * c; }
     template <int V>
-    struct State {
-        float p[V], b[V];
-    };
-    __device__ __forceinline__ Row begin_row(const PieceInfo& pc) const { return Row{pc.key}; }
-    template <int V>
-    __device__ __forceinline__ void load(const Row& r, int64_t col, State<V>& s) const
-    {
-        const int64_t off = r.key * c + col;
-        ld_state<V>(P.p + off, s.p);
-        if (P.buf) ld_state<V>(P.buf + off, s.b);
-    }
-    template <int V>
-    __device__ __forceinline__ void apply(const Row& r, int64_t col, State<V>& s, const float (&g)[V]) const
+    __device__ __forceinline__ void apply(const Row& r, int64_t col, float (&x)[kArrays][V], const float (&g)[V]) const
     {
         const int64_t off = r.key * c + col;
 #pragma unroll
-        for (int i = 0; i < V; ++i) sgd_coord(P, g[i], s.p[i], s.b[i]);
-        st_state<V>(P.p + off, s.p);
-        if (P.buf) st_state<V>(P.buf + off, s.b);
+        for (int i = 0; i < V; ++i) sgd_coord(P, g[i], x[0][i], x[1][i]);
+        st_state<V>(P.p + off, x[0]);
+        if (P.buf) st_state<V>(P.buf + off, x[1]);
     }
     __device__ __forceinline__ void end_row(const Row&, int, unsigned) const {}
 };
@@ -305,18 +311,19 @@ struct SgdEpi {
 // canonicalisation: write the summed row u
 struct StoreEpi {
     static constexpr const char* kName = "fused_rows_sum";
+    static constexpr int kArrays = 1;   // no state; one dummy array keeps the types simple
     StoreParams P;
     int64_t c;
     struct Row {
         int64_t u;
     };
+    __device__ __forceinline__ const int64_t* stage_last(const PieceInfo&) const { return nullptr; }
+    __device__ __forceinline__ Row make_row(const PieceInfo& pc, int64_t) const { return Row{pc.u}; }
+    __device__ __forceinline__ int arrays() const { return 0; }
+    __device__ __forceinline__ float* array(int) const { return nullptr; }
+    __device__ __forceinline__ int64_t base(const PieceInfo&) const { return 0; }
     template <int V>
-    struct State {};
-    __device__ __forceinline__ Row begin_row(const PieceInfo& pc) const { return Row{pc.u}; }
-    template <int V>
-    __device__ __forceinline__ void load(const Row&, int64_t, State<V>&) const {}
-    template <int V>
-    __device__ __forceinline__ void apply(const Row& r, int64_t col, State<V>&, const float (&g)[V]) const
+    __device__ __forceinline__ void apply(const Row& r, int64_t col, float (&)[kArrays][V], const float (&g)[V]) const
     {
         st_state<V>(P.out + r.u * c + col, g);
     }
@@ -324,84 +331,217 @@ struct StoreEpi {
 };
 
 // ------------------------------------------------------------ the kernel
-// Sum the gradient rows of entries [start, end) at this lane's columns of the
-// chunk starting at col0.  The first entry initialises the sum (so a lone value
-// passes through bit for bit); the compensation starts at -0.0 (s + -0.0 == s).
-template <int T, int NV, int V, class Src>
-__device__ __forceinline__ void sum_piece(const Src& src, const float* __restrict__ vals, int64_t c,
-                                          int64_t col0, int tl, const PieceInfo& pc, float (&s)[NV][V],
-                                          float (&cm)[NV][V])
+// First gradient row of a piece at this lane's columns of the chunk at col0.
+// It initialises the sum (a lone value passes through bit for bit); the
+// compensation starts at -0.0 (s + -0.0 == s).
+template <int T, int NV, int V>
+__device__ __forceinline__ void first_row(const float* __restrict__ vals, int64_t c, int64_t col0, int tl,
+                                          uint32_t perm0, float (&s)[NV][V], float (&cm)[NV][V])
 {
-    constexpr int B = NV >= kGradBatch ? 1 : kGradBatch / NV;   // gradient rows in flight per lane
+    const float* row = vals + static_cast<int64_t>(perm0) * c;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+        if (col < c) ld_grad<V>(row + col, s[k]);
+#pragma unroll
+        for (int i = 0; i < V; ++i) cm[k][i] = -0.0f;
+    }
+}
+
+// Input positions of the entries after the first of a piece (fewer than
+// 2*kPieceLen of them), spread over the team and loaded in one round trip:
+// lane tl holds entries start+1+tl, start+1+tl+T, ...  Teams of fewer than 8
+// lanes read each position when they use it.
+template <int T>
+struct PiecePerms {
+    static constexpr int kPerLane = T >= 8 ? (2 * kPieceLen - 2 + T - 1) / T : 1;
+    uint32_t pm[kPerLane];
+    template <class Src>
+    __device__ __forceinline__ void load(const Src& src, const PieceInfo& pc, int tl)
     {
-        const float* row = vals + static_cast<int64_t>(pc.perm0) * c;
+        if constexpr (T >= 8) {
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-            if (col < c) ld_grad<V>(row + col, s[k]);
-#pragma unroll
-            for (int i = 0; i < V; ++i) cm[k][i] = -0.0f;
+            for (int k = 0; k < kPerLane; ++k) {
+                const int64_t e = pc.start + 1 + tl + k * T;
+                pm[k] = (e < pc.end) ? src.perm(e) : 0u;
+            }
         }
     }
-    for (int64_t e = pc.start + 1; e < pc.end; e += B) {
-        uint32_t pe[B];
+    // every lane of the team calls with the same e
+    template <class Src>
+    __device__ __forceinline__ uint32_t get(const Src& src, const PieceInfo& pc, int64_t e, unsigned tmask) const
+    {
+        if constexpr (T >= 8) {
+            const int i = static_cast<int>(e - pc.start - 1);
+            uint32_t v = pm[0];
 #pragma unroll
-        for (int b = 0; b < B; ++b) pe[b] = (e + b < pc.end) ? src.perm(e + b) : 0u;
-        float x[B][NV][V];
+            for (int k = 1; k < kPerLane; ++k)
+                if (i / T == k) v = pm[k];
+            return __shfl_sync(tmask, v, i % T, T);
+        } else {
+            return src.perm(e);
+        }
+    }
+};
+
+// Gradient rows start+1 .. end-1 of a piece, ILP rows requested at once, added
+// in entry order with TwoSum compensation.
+template <int T, int NV, int V, int ILP, class Src>
+__device__ __forceinline__ void sum_rest(const Src& src, const PiecePerms<T>& pp, const float* __restrict__ vals,
+                                         int64_t c, int64_t col0, int tl, unsigned tmask, const PieceInfo& pc,
+                                         float (&s)[NV][V], float (&cm)[NV][V])
+{
+    constexpr int R = NV >= ILP ? 1 : ILP / NV;
+    for (int64_t e0 = pc.start + 1; e0 < pc.end; e0 += R) {
+        float x[R][NV][V];
 #pragma unroll
-        for (int b = 0; b < B; ++b) {
-            if (e + b < pc.end) {
-                const float* row = vals + static_cast<int64_t>(pe[b]) * c;
+        for (int r = 0; r < R; ++r) {
+            const int64_t e = e0 + r;
+            if (e < pc.end) {
+                const float* row = vals + static_cast<int64_t>(pp.get(src, pc, e, tmask)) * c;
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
                     const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                    if (col < c) ld_grad<V>(row + col, x[b][k]);
+                    if (col < c) ld_grad<V>(row + col, x[r][k]);
                 }
             }
         }
 #pragma unroll
-        for (int b = 0; b < B; ++b) {
-            if (e + b < pc.end) {
+        for (int r = 0; r < R; ++r) {
+            if (e0 + r < pc.end) {
 #pragma unroll
                 for (int k = 0; k < NV; ++k)
 #pragma unroll
-                    for (int i = 0; i < V; ++i) two_sum_acc(s[k][i], cm[k][i], x[b][k][i]);
+                    for (int i = 0; i < V; ++i) two_sum_acc(s[k][i], cm[k][i], x[r][k][i]);
             }
         }
     }
 }
 
-// Slot of level-0 piece i (i-th piece, in sorted order) of the segment starting
-// at sorted position s0.  Pieces after the first start at multiples of
-// kPieceLen, so piece i >= 1 takes slot s0/kPieceLen + i; the first piece takes
-// slot s0/kPieceLen when it starts on a multiple, else nb + s0/kPieceLen (only
-// one segment can cross out of a block of kPieceLen positions).  2*nb slots.
+// Pieces of a segment [s0, s1) and their partial-sum slots.  The first piece
+// starts at s0; piece i >= 1 starts at q1 + (i-1)*kPieceLen, where q1 is the
+// smallest multiple of kPieceLen >= s0 + kPieceLen (see run detection).  Piece
+// i >= 1 takes slot q1/kPieceLen + i - 1 (one per boundary position); the first
+// piece takes slot s0/kPieceLen when s0 is a multiple, else nb + s0/kPieceLen
+// (a split segment is longer than kPieceLen, so no two of them start in the same
+// block of kPieceLen positions).  2*nb slots in all.
 struct SlotMap {
-    int64_t b0, first;
+    int64_t q1b, first;
     __device__ __forceinline__ SlotMap(int64_t s0, int64_t nb)
-        : b0(s0 / kPieceLen), first((s0 % kPieceLen == 0) ? s0 / kPieceLen : nb + s0 / kPieceLen) {}
-    __device__ __forceinline__ int64_t operator()(int64_t i) const { return i == 0 ? first : b0 + i; }
+        : q1b((s0 + 2 * kPieceLen - 1) / kPieceLen),
+          first((s0 % kPieceLen == 0) ? s0 / kPieceLen : nb + s0 / kPieceLen) {}
+    __device__ __forceinline__ int64_t operator()(int64_t i) const { return i == 0 ? first : q1b + i - 1; }
+    __device__ __forceinline__ int64_t pieces(int64_t s1) const
+    {
+        const int64_t q1 = q1b * kPieceLen;
+        return (s1 - 1 >= q1) ? 2 + (s1 - 1 - q1) / kPieceLen : 1;
+    }
+    __device__ __forceinline__ int64_t index(int64_t start, int64_t s0) const
+    {
+        return start == s0 ? 0 : start / kPieceLen - q1b + 1;
+    }
 };
 
-// Combining tree of a multi-piece segment, entered after this team has written
-// its level-0 partial.  At each level the team bumps its group's counter; only
-// the last of the group to arrive continues: it sums the group's partials in
-// slot order into the slot of the group's first member (whose partial it has
-// just consumed), and at the top level applies the update instead.
+// Loads the optimizer state of one row chunk (the live arrays of the epilogue).
+template <int T, int NV, int V, class Epi>
+__device__ __forceinline__ void load_state(const Epi& epi, const PieceInfo& pc, int64_t c, int64_t col0, int tl,
+                                           float (&x)[NV][Epi::kArrays][V])
+{
+    const int na = epi.arrays();
+    const int64_t rb = epi.base(pc);
+#pragma unroll
+    for (int a = 0; a < Epi::kArrays; ++a) {
+        if (a < na) {
+            const float* arr = epi.array(a) + rb;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+                if (col < c) ld_state<V>(arr + col, x[k][a]);
+            }
+        }
+    }
+}
+
+// Sums a piece's gradient rows and applies the update to its row (a piece that
+// holds its whole segment).  The row's state, last_step and first gradient row
+// are requested together, before any of them is used.
 template <int T, int NV, int V, class Src, class Epi>
-__device__ __forceinline__ void combine_tree(const Src& src, int64_t c, const Epi& epi, float* __restrict__ part,
-                                             uint32_t* __restrict__ lvl_cnt, int64_t nb, const PieceInfo& pc,
-                                             int tl, unsigned tmask)
+__device__ __forceinline__ void apply_single(const Src& src, const float* __restrict__ vals, int64_t c,
+                                             const Epi& epi, const PieceInfo& pc, int tl, unsigned tmask)
 {
     constexpr int CW = T * NV * V;
+    constexpr int A = Epi::kArrays;
+    const int nchunks = static_cast<int>((c + CW - 1) / CW);
+    const int64_t* lp = epi.stage_last(pc);
+    int64_t last = 0;
+    PiecePerms<T> pp;
+    if (pc.end - pc.start > 1) pp.load(src, pc, tl);
+    for (int cc = 0; cc < nchunks; ++cc) {
+        const int64_t col0 = static_cast<int64_t>(cc) * CW;
+        float x[NV][A][V];
+        load_state<T, NV, V>(epi, pc, c, col0, tl, x);
+        if (cc == 0 && lp) last = *lp;
+        float s[NV][V], cm[NV][V];
+        first_row<T, NV, V>(vals, c, col0, tl, pc.perm0, s, cm);
+        if (pc.end - pc.start > 1) sum_rest<T, NV, V, kRowIlp>(src, pp, vals, c, col0, tl, tmask, pc, s, cm);
+        const typename Epi::Row row = epi.make_row(pc, last);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+            if (col < c) {
+                float g[V];
+#pragma unroll
+                for (int i = 0; i < V; ++i) g[i] = __fadd_rn(s[k][i], cm[k][i]);
+                epi.template apply<V>(row, col, x[k], g);
+            }
+        }
+    }
+    epi.end_row(epi.make_row(pc, last), tl, tmask);
+}
+
+// A piece of a multi-piece segment: its compensated partial sum goes to its
+// level-0 slot; then, level by level, the team bumps its group's counter and
+// only the last of the group to arrive continues: it sums the group's partials
+// in slot order into the slot of the group's first member (whose partial it has
+// just consumed), and at the top level applies the update instead.  The order
+// of every addition is fixed by the slots, whichever team arrives last.  Out of
+// line: it runs for few pieces, and its registers stay out of the budget of the
+// single-piece path.
+template <int T, int NV, int V, class Src, class Epi>
+__device__ __noinline__ void apply_multi(const Src& src, const float* __restrict__ vals, int64_t c,
+                                            const Epi& epi, float* __restrict__ part,
+                                            uint32_t* __restrict__ lvl_cnt, int64_t nb, const PieceInfo pc,
+                                            int tl, unsigned tmask)
+{
+    constexpr int CW = T * NV * V;
+    constexpr int A = Epi::kArrays;
     const int nchunks = static_cast<int>((c + CW - 1) / CW);
     const int64_t nslots = 2 * nb;
     int64_t s0, s1;
     src.seg_bounds(pc.u, s0, s1);
     const SlotMap slot_of(s0, nb);
-    int64_t Kl = 1 + (s1 - 1) / kPieceLen - slot_of.b0;   // items at this level
-    int64_t kl = (pc.start == s0) ? 0 : pc.start / kPieceLen - slot_of.b0;
-    int64_t stride = 1;                                   // level-0 pieces per item
+    int64_t Kl = slot_of.pieces(s1);          // items at this level
+    int64_t kl = slot_of.index(pc.start, s0);
+    {
+        float* ps = part + slot_of(kl) * 2 * c;
+        PiecePerms<T> pp;
+        pp.load(src, pc, tl);
+        for (int cc = 0; cc < nchunks; ++cc) {
+            const int64_t col0 = static_cast<int64_t>(cc) * CW;
+            float s[NV][V], cm[NV][V];
+            first_row<T, NV, V>(vals, c, col0, tl, pc.perm0, s, cm);
+            sum_rest<T, NV, V, 2 * kRowIlp>(src, pp, vals, c, col0, tl, tmask, pc, s, cm);
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+                if (col < c) {
+                    st_part<V>(ps + col, s[k]);
+                    st_part<V>(ps + c + col, cm[k]);
+                }
+            }
+        }
+    }
+    int64_t stride = 1;                        // level-0 pieces per item of this level
     for (int lvl = 0;; ++lvl) {
         __threadfence();
         __syncwarp(tmask);
@@ -415,51 +555,65 @@ __device__ __forceinline__ void combine_tree(const Src& src, int64_t c, const Ep
         __threadfence();
         const int64_t Knext = (Kl + kGroup - 1) / kGroup;
         const bool final = (Knext == 1);
-        typename Epi::Row row{};
-        if (final) row = epi.begin_row(pc);
+        const int64_t* lp = final ? epi.stage_last(pc) : nullptr;
+        const int64_t last = lp ? *lp : 0;
         for (int cc = 0; cc < nchunks; ++cc) {
             const int64_t col0 = static_cast<int64_t>(cc) * CW;
             float S[NV][V], C[NV][V];
-            typename Epi::template State<V> st[NV];
-            if (final) {
+            constexpr int MR = NV >= 4 ? 1 : 4 / NV;   // partials requested at once
+            for (int64_t m0 = 0; m0 < members; m0 += MR) {
+                float xs[MR][NV][V], xc[MR][NV][V];
 #pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                    if (col < c) epi.template load<V>(row, col, st[k]);
-                }
-            }
-            for (int64_t mi = 0; mi < members; ++mi) {
-                const float* ps = part + (slot_of((g * kGroup + mi) * stride) * 2) * c;
+                for (int r = 0; r < MR; ++r) {
+                    if (m0 + r < members) {
+                        const float* ps = part + (slot_of((g * kGroup + m0 + r) * stride) * 2) * c;
 #pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                    if (col < c) {
-                        float xs[V], xc[V];
-                        ld_part<V>(ps + col, xs);
-                        ld_part<V>(ps + c + col, xc);
-#pragma unroll
-                        for (int i = 0; i < V; ++i) {
-                            if (mi == 0) {
-                                S[k][i] = xs[i];
-                                C[k][i] = xc[i];
-                            } else {
-                                two_sum_merge(S[k][i], C[k][i], xs[i], xc[i]);
+                        for (int k = 0; k < NV; ++k) {
+                            const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+                            if (col < c) {
+                                ld_part<V>(ps + col, xs[r][k]);
+                                ld_part<V>(ps + c + col, xc[r][k]);
                             }
                         }
                     }
                 }
-            }
-            float* pd = part + (lead_slot * 2) * c;
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                if (col < c) {
-                    if (final) {
+                for (int r = 0; r < MR; ++r) {
+                    if (m0 + r < members) {
+#pragma unroll
+                        for (int k = 0; k < NV; ++k)
+#pragma unroll
+                            for (int i = 0; i < V; ++i) {
+                                if (m0 + r == 0) {
+                                    S[k][i] = xs[r][k][i];
+                                    C[k][i] = xc[r][k][i];
+                                } else {
+                                    two_sum_merge(S[k][i], C[k][i], xs[r][k][i], xc[r][k][i]);
+                                }
+                            }
+                    }
+                }
+            }
+            if (final) {
+                float x[NV][A][V];
+                load_state<T, NV, V>(epi, pc, c, col0, tl, x);
+                const typename Epi::Row row = epi.make_row(pc, last);
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+                    if (col < c) {
                         float gsum[V];
 #pragma unroll
                         for (int i = 0; i < V; ++i) gsum[i] = __fadd_rn(S[k][i], C[k][i]);
-                        epi.template apply<V>(row, col, st[k], gsum);
-                    } else {
+                        epi.template apply<V>(row, col, x[k], gsum);
+                    }
+                }
+            } else {
+                float* pd = part + (lead_slot * 2) * c;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+                    if (col < c) {
                         st_part<V>(pd + col, S[k]);
                         st_part<V>(pd + c + col, C[k]);
                     }
@@ -467,7 +621,7 @@ __device__ __forceinline__ void combine_tree(const Src& src, int64_t c, const Ep
             }
         }
         if (final) {
-            epi.end_row(row, tl, tmask);
+            epi.end_row(epi.make_row(pc, last), tl, tmask);
             return;
         }
         kl = g;
@@ -476,6 +630,10 @@ __device__ __forceinline__ void combine_tree(const Src& src, int64_t c, const Ep
     }
 }
 
+// Teams first take the pieces of multi-piece segments (from the list run
+// detection built, so these longer dependency chains start first and overlap
+// the other teams' streaming), then the single pieces.  Work is handed out by
+// atomic tickets on a raw input, statically on a canonical one.
 template <int T, int NV, int V, class Src, class Epi>
 __global__ void __launch_bounds__(kBlock, kFusedMinBlocks) k_fused_rows(Src src, const float* __restrict__ vals,
                                                                         int64_t c, Epi epi, float* __restrict__ part,
@@ -483,60 +641,41 @@ __global__ void __launch_bounds__(kBlock, kFusedMinBlocks) k_fused_rows(Src src,
                                                                         int32_t* d_err)
 {
     if (read_error(d_err)) return;
-    constexpr int CW = T * NV * V;
     constexpr int kTeams = kBlock / T;
     const int lane = threadIdx.x & 31;
     const int tl = lane & (T - 1);
     const unsigned tmask = (T == 32) ? kFull : (((1u << T) - 1u) << (lane & ~(T - 1)));
+    const int64_t team_g = static_cast<int64_t>(blockIdx.x) * kTeams + threadIdx.x / T;
     const int64_t nteams = static_cast<int64_t>(gridDim.x) * kTeams;
     const int64_t P = src.count();
-    const int nchunks = static_cast<int>((c + CW - 1) / CW);
-
-    for (int64_t j = static_cast<int64_t>(blockIdx.x) * kTeams + threadIdx.x / T; j < P; j += nteams) {
-        const PieceInfo pc = src.piece(j);
-        // single: the whole segment is this piece -> update directly;
-        // multi: write this piece's compensated partial to its level-0 slot
-        typename Epi::Row row{};
-        if (!pc.multi) row = epi.begin_row(pc);
-        float* ps = nullptr;
-        if (pc.multi) {
-            int64_t s0, s1;
-            src.seg_bounds(pc.u, s0, s1);
-            const SlotMap slot_of(s0, nb);
-            ps = part + slot_of(pc.start == s0 ? 0 : pc.start / kPieceLen - slot_of.b0) * 2 * c;
+    if constexpr (Src::kTickets) {
+        // dynamic: multi pieces one per ticket until they run out, then single
+        // pieces kTicketChunk per ticket, so teams held up by a multi piece take
+        // fewer single pieces
+        const int64_t M = src.count_multi();
+        while (true) {
+            uint32_t t = 0;
+            if (tl == 0) t = atomicAdd(src.ticket(kTicketM), 1u);
+            t = __shfl_sync(tmask, t, 0, T);
+            if (t >= M) break;
+            apply_multi<T, NV, V>(src, vals, c, epi, part, lvl_cnt, nb, src.piece(src.multi_index(t)), tl, tmask);
         }
-        for (int cc = 0; cc < nchunks; ++cc) {
-            const int64_t col0 = static_cast<int64_t>(cc) * CW;
-            typename Epi::template State<V> st[NV];
-            if (!pc.multi) {
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                    if (col < c) epi.template load<V>(row, col, st[k]);
-                }
-            }
-            float s[NV][V], cm[NV][V];
-            sum_piece<T, NV, V>(src, vals, c, col0, tl, pc, s, cm);
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                if (col < c) {
-                    if (!pc.multi) {
-                        float g[V];
-#pragma unroll
-                        for (int i = 0; i < V; ++i) g[i] = __fadd_rn(s[k][i], cm[k][i]);
-                        epi.template apply<V>(row, col, st[k], g);
-                    } else {
-                        st_part<V>(ps + col, s[k]);
-                        st_part<V>(ps + c + col, cm[k]);
-                    }
-                }
+        while (true) {
+            uint32_t t = 0;
+            if (tl == 0) t = atomicAdd(src.ticket(kTicketS), 1u);
+            t = __shfl_sync(tmask, t, 0, T);
+            const int64_t j0 = static_cast<int64_t>(t) * kTicketChunk;
+            if (j0 >= P) break;
+            const int64_t j1 = (j0 + kTicketChunk) < P ? j0 + kTicketChunk : P;
+            for (int64_t j = j0; j < j1; ++j) {
+                const PieceInfo pc = src.piece(j);
+                if (!pc.multi) apply_single<T, NV, V>(src, vals, c, epi, pc, tl, tmask);
             }
         }
-        if (!pc.multi)
-            epi.end_row(row, tl, tmask);
-        else
-            combine_tree<T, NV, V>(src, c, epi, part, lvl_cnt, nb, pc, tl, tmask);
+    } else {
+        (void)nteams;
+        for (int64_t j = team_g; j < P; j += nteams)
+            apply_single<T, NV, V>(src, vals, c, epi, src.piece(j), tl, tmask);
     }
 }
 
@@ -559,7 +698,8 @@ cudaError_t launch_shape(const Src& src, int64_t max_pieces, const float* vals, 
 }
 
 // Team shape: smallest power-of-two team that covers a row with one vector per
-// lane; rows wider than 32 vectors give each lane up to 8 vectors per chunk.
+// lane; rows wider than 32 vectors give each lane 2 vectors per chunk and are
+// walked in chunks of 256 (or 128 scalar) columns.
 template <class Src, class Epi>
 cudaError_t launch_fused(const Src& src, int64_t max_pieces, const float* vals, int64_t c, const Epi& epi,
                          float* part, uint32_t* lvl_cnt, int64_t nb, int vec4, int32_t* d_err,
@@ -575,9 +715,7 @@ cudaError_t launch_fused(const Src& src, int64_t max_pieces, const float* vals, 
         if (nv <= 8) return SO_LAUNCH(8, 1, 4);
         if (nv <= 16) return SO_LAUNCH(16, 1, 4);
         if (nv <= 32) return SO_LAUNCH(32, 1, 4);
-        if (nv <= 64) return SO_LAUNCH(32, 2, 4);
-        if (nv <= 128) return SO_LAUNCH(32, 4, 4);
-        return SO_LAUNCH(32, 8, 4);
+        return SO_LAUNCH(32, 2, 4);   // wider rows: chunks of 256 columns
     }
     if (c <= 1) return SO_LAUNCH(1, 1, 1);
     if (c <= 2) return SO_LAUNCH(2, 1, 1);
@@ -591,7 +729,7 @@ cudaError_t launch_fused(const Src& src, int64_t max_pieces, const float* vals, 
 
 inline SortedSrc sorted_src(const SortWs& ws)
 {
-    return SortedSrc{ws.rec, ws.vals[ws.final_buf], ws.seg_off, ws.counts};
+    return SortedSrc{ws.rec, ws.vals[ws.final_buf], ws.seg_off, ws.mlist, ws.counts};
 }
 
 }  // namespace so

@@ -65,6 +65,7 @@ WsLayout ws_layout(int64_t n, int64_t c, int64_t bound)
     L.vals1 = take(sizeof(uint32_t) * n);
     L.rec = take(sizeof(uint4) * (size_t)(n + L.nb + 2));
     L.seg_off = take(sizeof(uint32_t) * (size_t)(n + 1));
+    L.mlist = take(sizeof(uint32_t) * (size_t)(n + L.nb + 2));
     L.part = take(sizeof(float) * (size_t)(2 * L.nb) * 2 * (size_t)c);
     off = align_up(off, 256);
     L.ctrl_begin = off;
@@ -88,6 +89,7 @@ SortWs carve(const WsLayout& L, void* ws)
     w.vals[1] = reinterpret_cast<uint32_t*>(b + L.vals1);
     w.rec = reinterpret_cast<uint4*>(b + L.rec);
     w.seg_off = reinterpret_cast<uint32_t*>(b + L.seg_off);
+    w.mlist = reinterpret_cast<uint32_t*>(b + L.mlist);
     w.part = reinterpret_cast<float*>(b + L.part);
     w.gh = reinterpret_cast<uint32_t*>(b + L.gh);
     w.counts = reinterpret_cast<uint32_t*>(b + L.counts);
@@ -101,7 +103,11 @@ SortWs carve(const WsLayout& L, void* ws)
 // ---------------------------------------------------------------------- K1
 // Range check (0 <= idx < bound) and the digit histograms of all passes.  Every
 // key is counted, valid or not, with the same truncation the radix passes use,
-// so the scatter offsets stay inside [0, n) whatever the input.
+// so the scatter offsets stay inside [0, n) whatever the input.  Each thread
+// requests its kHistItems keys at once (128-bit loads when aligned), then
+// counts them in shared memory; one global atomic per non-empty bin and block.
+constexpr int kHistItems = 8;
+
 __global__ void __launch_bounds__(kBlock) k_range_hist(const int64_t* __restrict__ idx, uint32_t n,
                                                        int64_t bound, int passes,
                                                        uint32_t* __restrict__ gh, int32_t* d_err)
@@ -110,12 +116,28 @@ __global__ void __launch_bounds__(kBlock) k_range_hist(const int64_t* __restrict
     for (int i = threadIdx.x; i < kMaxPasses * 256; i += kBlock) sh[i] = 0;
     __syncthreads();
     int bad = 0;
-    const uint32_t stride = gridDim.x * kBlock;
-    for (uint32_t i = blockIdx.x * kBlock + threadIdx.x; i < n; i += stride) {
-        const int64_t k = idx[i];
-        bad |= (k < 0) | (k >= bound);
-        const uint32_t key = static_cast<uint32_t>(static_cast<uint64_t>(k));
-        for (int p = 0; p < passes; ++p) atomicAdd(&sh[p * 256 + ((key >> (8 * p)) & 255u)], 1u);
+    const uint32_t stride = gridDim.x * kBlock * kHistItems;
+    for (uint32_t i0 = (blockIdx.x * kBlock + threadIdx.x) * kHistItems; i0 < n; i0 += stride) {
+        int64_t k[kHistItems];
+        if (i0 + kHistItems <= n && (reinterpret_cast<uintptr_t>(idx + i0) & 15u) == 0) {
+#pragma unroll
+            for (int j = 0; j < kHistItems; j += 2) {
+                const longlong2 q = *reinterpret_cast<const longlong2*>(idx + i0 + j);
+                k[j] = q.x;
+                k[j + 1] = q.y;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < kHistItems; ++j) k[j] = (i0 + j < n) ? idx[i0 + j] : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < kHistItems; ++j) {
+            if (i0 + j < n) {
+                bad |= (k[j] < 0) | (k[j] >= bound);
+                const uint32_t key = static_cast<uint32_t>(static_cast<uint64_t>(k[j]));
+                for (int p = 0; p < passes; ++p) atomicAdd(&sh[p * 256 + ((key >> (8 * p)) & 255u)], 1u);
+            }
+        }
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) set_error(d_err, SPARSE_ERR_INDEX_OUT_OF_RANGE);
     for (int i = threadIdx.x; i < passes * 256; i += kBlock) {
@@ -215,14 +237,32 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
     s_texcl[tid] = block_excl_scan(tcount, s_scan, &total);
     const uint32_t gexcl = block_excl_scan(gh[tid], s_scan, &total);
 
+    // look-back: kLook predecessor words per round trip, consumed nearest first
+    // until an inclusive one; a word not yet published stops the round (its
+    // tile started earlier, so it publishes soon) and is read again.
+    constexpr int kLook = 4;
     uint32_t excl = 0;
     if (tile > 0) {
         int64_t j = static_cast<int64_t>(tile) - 1;
         uint32_t spins = 0;
-        while (j >= 0) {
-            const uint32_t w = ld_volatile(status + static_cast<size_t>(j) * 256 + tid);
-            const uint32_t flag = w & 3u;
-            if (flag == 0u) {
+        bool done = false;
+        while (!done && j >= 0) {
+            uint32_t w[kLook];
+#pragma unroll
+            for (int q = 0; q < kLook; ++q)
+                w[q] = (j - q >= 0) ? ld_volatile(status + static_cast<size_t>(j - q) * 256 + tid) : 2u;
+            int used = 0;
+#pragma unroll
+            for (int q = 0; q < kLook; ++q) {
+                if (done || used < q) break;
+                const uint32_t flag = w[q] & 3u;
+                if (flag == 0u) break;
+                excl += w[q] >> 2;
+                ++used;
+                if (flag == 2u) done = true;
+            }
+            if (done) break;
+            if (used == 0) {
                 if (++spins > kSpinLimit) {
                     set_error(d_err, SPARSE_ERR_INTERNAL);
                     break;
@@ -230,9 +270,7 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
                 if (spins > 64) __nanosleep(64);
                 continue;
             }
-            excl += w >> 2;
-            if (flag == 2u) break;
-            --j;
+            j -= used;
         }
         st_volatile(my, ((excl + tcount) << 2) | 2u);
     }
@@ -260,17 +298,25 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
 
 // ---------------------------------------------------------------------- K3
 // Run detection over the sorted keys.  Position q is a segment head when it is
-// the first position or its key differs from the previous one; it is a piece
-// head when it is a segment head or q % kPieceLen == 0.  Each piece covers at
-// most kPieceLen sorted entries of one segment.  Outputs (u = segment index,
+// the first position or its key differs from the previous one.  It is a piece
+// head when it is a segment head, or when q is a multiple of kPieceLen and
+// position q - kPieceLen belongs to the same segment.  So a segment of at most
+// kPieceLen entries is always one piece (wherever it lies), and a longer one is
+// cut at the multiples of kPieceLen that lie at least kPieceLen past its start:
+// its first piece holds kPieceLen .. 2*kPieceLen-1 entries, the others at most
+// kPieceLen.  Outputs (u = segment index,
 // j = piece index):
 //   seg_off[u] = first sorted position of segment u, seg_off[U] = n
 //   rec[j] = {start, key, u | kMultiFlag if the segment spans several pieces,
 //             input position of the start}, rec[P] = {n, 0, 0, 0}
+//   mlist[0 .. M) = the indices j of the multi-piece pieces, in no particular
+//             order (appended through an atomic counter; the order in which
+//             they are processed does not affect any result)
 // Status word of a tile: flag << 62 | heads << 31 | pieces.
 __global__ void __launch_bounds__(kBlock) k_run_detect(
     const uint32_t* __restrict__ skey, const uint32_t* __restrict__ sperm, uint32_t n,
-    uint4* __restrict__ rec, uint32_t* __restrict__ seg_off, unsigned long long* dstatus,
+    uint4* __restrict__ rec, uint32_t* __restrict__ seg_off, uint32_t* __restrict__ mlist,
+    unsigned long long* dstatus,
     uint32_t* tile_ctr, uint32_t* counts, int64_t* __restrict__ idx_out,
     int64_t* __restrict__ seg_off_out, int64_t* __restrict__ perm_out, int64_t* d_nnz_out,
     const int64_t* __restrict__ ls, int ls_per_coord, int64_t c, int64_t bound, int64_t t,
@@ -299,6 +345,12 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
 #pragma unroll
         for (int i = 0; i < kRunItems; ++i) k[i] = (p0 + i < n) ? skey[p0 + i] : 0u;
     }
+    // a multiple q of kPieceLen inside a segment starts a new piece only when the
+    // segment already holds position q - kPieceLen (kRunItems divides kPieceLen:
+    // at most the first item of a thread is such a multiple)
+    static_assert(kPieceLen % kRunItems == 0, "piece boundaries fall on a thread's first item");
+    const bool at_boundary = (p0 < n) && (p0 % kPieceLen == 0) && p0 >= kPieceLen;
+    const uint32_t key_back = at_boundary ? skey[p0 - kPieceLen] : 0u;
     uint32_t headm = 0, piecem = 0;
 #pragma unroll
     for (int i = 0; i < kRunItems; ++i) {
@@ -307,7 +359,8 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
             const uint32_t before = (i == 0) ? prev : k[i - 1];
             const bool h = (q == 0) || (k[i] != before);
             headm |= (h ? 1u : 0u) << i;
-            piecem |= ((h || (q % kPieceLen) == 0) ? 1u : 0u) << i;
+            const bool split = (i == 0) && at_boundary && !h && key_back == k[0];
+            piecem |= ((h || split) ? 1u : 0u) << i;
         }
     }
     const uint32_t hc = __popc(headm), pc = __popc(piecem);
@@ -355,6 +408,30 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     uint32_t h_run = static_cast<uint32_t>(ex >> 31) + (xe >> 16);       // heads before p0
     uint32_t p_run = static_cast<uint32_t>(ex & 0x7fffffffull) + (xe & 0xffffu);
 
+    // everything the items below read is requested first: input positions,
+    // the key at the next piece boundary of each segment head, last_step
+    uint32_t pmv[kRunItems];
+    if (p0 + kRunItems <= n) {
+        const uint4 a = *reinterpret_cast<const uint4*>(sperm + p0);
+        const uint4 b = *reinterpret_cast<const uint4*>(sperm + p0 + 4);
+        pmv[0] = a.x; pmv[1] = a.y; pmv[2] = a.z; pmv[3] = a.w;
+        pmv[4] = b.x; pmv[5] = b.y; pmv[6] = b.z; pmv[7] = b.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < kRunItems; ++i) pmv[i] = (p0 + i < n) ? sperm[p0 + i] : 0u;
+    }
+    uint32_t nxt_key[kRunItems];
+    int64_t last[kRunItems];
+#pragma unroll
+    for (int i = 0; i < kRunItems; ++i) {
+        const uint32_t q = p0 + i;
+        const bool h = (headm >> i) & 1u;
+        // first boundary that can split a segment starting at q: the smallest
+        // multiple of kPieceLen that is >= q + kPieceLen
+        const uint32_t nxt = (q + 2 * kPieceLen - 1) / kPieceLen * kPieceLen;
+        nxt_key[i] = (h && nxt < n) ? skey[nxt] : ~k[i];
+        last[i] = (h && ls && !ls_per_coord && static_cast<int64_t>(k[i]) < bound) ? ls[k[i]] : 0;
+    }
 #pragma unroll
     for (int i = 0; i < kRunItems; ++i) {
         const uint32_t q = p0 + i;
@@ -368,7 +445,7 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
             if (seg_off_out) seg_off_out[u] = static_cast<int64_t>(q);
             if (ls && static_cast<int64_t>(k[i]) < bound) {
                 if (!ls_per_coord) {
-                    if (ls[k[i]] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                    if (last[i] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
                 } else {
                     const int64_t b = static_cast<int64_t>(k[i]) * c;
                     for (int64_t jc = 0; jc < c; ++jc)
@@ -379,15 +456,13 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
                 }
             }
         }
-        const uint32_t pm = sperm[q];
+        const uint32_t pm = pmv[i];
         if (perm_out) perm_out[q] = static_cast<int64_t>(pm);
         if ((piecem >> i) & 1u) {
             bool multi = true;
-            if (h) {
-                const uint32_t nxt = (q / kPieceLen + 1) * kPieceLen;
-                multi = (nxt < n) && (skey[nxt] == k[i]);
-            }
+            if (h) multi = (nxt_key[i] == k[i]);
             rec[p_run] = make_uint4(q, k[i], u | (multi ? kMultiFlag : 0u), pm);
+            if (multi) mlist[atomicAdd(counts + kCntM, 1u)] = p_run;
             ++p_run;
         }
     }
@@ -415,8 +490,8 @@ cudaError_t sort_and_segment(const int64_t* idx, int64_t n, int64_t c, int64_t b
     }
     if (e != cudaSuccess) return e;
     const uint32_t nn = static_cast<uint32_t>(n);
-    const int hist_blocks =
-        static_cast<int>(std::min<int64_t>((n + kBlock * 16 - 1) / (kBlock * 16), 4 * num_sms()));
+    const int hist_blocks = static_cast<int>(
+        std::min<int64_t>((n + kBlock * kHistItems - 1) / (kBlock * kHistItems), 2 * num_sms()));
     {
         SO_PROFILE("range_hist", s);
         k_range_hist<<<hist_blocks, kBlock, 0, s>>>(idx, nn, bound, L.passes, ws.gh, d_err);
@@ -438,7 +513,7 @@ cudaError_t sort_and_segment(const int64_t* idx, int64_t n, int64_t c, int64_t b
     }
     SO_PROFILE("run_detect", s);
     k_run_detect<<<L.run_tiles, kBlock, 0, s>>>(ws.keys[ws.final_buf], ws.vals[ws.final_buf], nn, ws.rec,
-                                                ws.seg_off, ws.dstatus, ws.counts + kCtrRun, ws.counts,
+                                                ws.seg_off, ws.mlist, ws.dstatus, ws.counts + kCtrRun, ws.counts,
                                                 idx_out, seg_off_out, perm_out, d_nnz_out, ls, ls_per_coord,
                                                 c, bound, t, d_err);
     return cudaGetLastError();
