@@ -2,6 +2,8 @@
 // translation units of libsparseopt (sm_103a).
 #pragma once
 
+#include <utility>
+
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -10,17 +12,59 @@
 
 namespace so {
 
+// ---------------------------------------------------------------- launches
+// Every kernel of this library is launched with programmatic dependent launch
+// allowed, and every kernel starts with pdl_enter(): it waits until the
+// previous kernel on the stream has completed and its memory is visible
+// (griddepcontrol.wait), then lets the next kernel's blocks be scheduled
+// (griddepcontrol.launch_dependents).  Results and stream order are those of
+// plain launches; what is saved is the launch latency between dependent
+// kernels, since the next grid is already resident when the wait returns.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <class... P, class... A>
+inline cudaError_t launch(void (*kernel)(P...), dim3 grid, dim3 block, cudaStream_t s, A&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+
+
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kBlock = 256;            // threads per block of every kernel here
 constexpr int kPieceLen = 32;          // L: sorted entries summed by one team before a partial
-constexpr int kGroup = 32;             // G: fan-in of the partial-combining tree
 constexpr int kSortItems = 8;          // keys per thread in a radix pass
 constexpr int kSortTile = kBlock * kSortItems;
 constexpr int kRunItems = 8;           // sorted entries per thread in run detection
 constexpr int kRunTile = kBlock * kRunItems;
 constexpr int kMaxPasses = 4;          // 8-bit digits, keys < 2^32
-constexpr uint32_t kSingleMask = 0x7fffffffu;
-constexpr uint32_t kMultiFlag = 0x80000000u;
+constexpr int kHistItems = 8;          // keys a histogram thread requests at once
+#ifndef SO_HIST_BLOCKS
+#define SO_HIST_BLOCKS 32
+#endif
+constexpr int kMaxHistBlocks = SO_HIST_BLOCKS;   // histogram blocks (each radix tile sums their counts)
+constexpr uint32_t kSingleMask = 0x3fffffffu;   // segment index bits of a piece record
+constexpr uint32_t kMultiFlag = 0x80000000u;    // piece of a segment split into several pieces
+constexpr uint32_t kLongFlag = 0x40000000u;     // whole segment of more than kShortLen entries
+// Pieces of at most kShortLen entries go to the short-piece kernel; longer ones
+// (and all pieces of split segments) to the long-piece kernel.
+#ifndef SO_SHORT_LEN
+#define SO_SHORT_LEN 4
+#endif
+constexpr int kShortLen = SO_SHORT_LEN;
 // Bounded waits on another block's published value: after this many polls the
 // waiting block records SPARSE_ERR_INTERNAL and carries on with a zero value.
 constexpr uint32_t kSpinLimit = 1u << 22;
@@ -117,15 +161,15 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* tmp, u
 // ------------------------------------------------------------ workspace map
 struct WsLayout {
     int64_t n, c, nb;
-    int passes, sort_tiles, run_tiles, levels;
-    size_t keys0, keys1, vals0, vals1, rec, seg_off, mlist, part;
-    size_t ctrl_begin, gh, counts, rstatus, dstatus, lvl_cnt, ctrl_end;
+    int passes, sort_tiles, run_tiles, hist_blocks;
+    size_t keys0, keys1, vals0, vals1, rec, seg_off, mlist, slist, part, bh;
+    size_t ctrl_begin, counts, rstatus, dstatus, ctrl_end;
     size_t total;
 };
 
 // counts[] word indices
-enum { kCtrHist = 0, kCtrPass0 = 1, kCtrRun = 5, kCntU = 8, kCntP = 9, kCntM = 10, kTicketM = 11, kTicketS = 12,
-       kCountsWords = 16 };
+enum { kCtrHist = 0, kCtrPass0 = 1, kCtrRun = 5, kCntU = 8, kCntP = 9, kCntM = 10, kCntS = 11, kTicketM = 12,
+       kTicketS = 13, kCountsWords = 16 };
 
 WsLayout ws_layout(int64_t n, int64_t c, int64_t bound);
 
@@ -135,13 +179,13 @@ struct SortWs {
     uint32_t* vals[2];
     uint4* rec;           // [P+1] piece records {start, key, u | multi, perm of start}
     uint32_t* seg_off;    // [U+1]
-    uint32_t* mlist;      // [M] indices of the pieces of multi-piece segments (any order)
+    uint32_t* mlist;      // [M] indices of the long pieces (any order)
+    uint32_t* slist;      // [S] indices of the first pieces of split segments (any order)
     float* part;          // partial sums: [2*nb slots][2][c]
-    uint32_t* gh;         // [4][256] digit histograms
-    uint32_t* counts;     // [16]: tile counters, U, P, M, work tickets of the fused kernel
+    uint32_t* bh;         // [hist_blocks][4][256] digit histograms, one set per block
+    uint32_t* counts;     // [16]: tile counters, U, P, M, S, work tickets
     uint32_t* rstatus;    // [passes][sort_tiles][256]
     unsigned long long* dstatus;  // [run_tiles]
-    uint32_t* lvl_cnt;    // [levels][2*nb]
     int final_buf;        // which keys/vals buffer holds the sorted result
 };
 

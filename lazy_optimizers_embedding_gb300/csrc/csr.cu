@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict_
                                                       const int64_t* __restrict__ ls, int ls_per_coord,
                                                       int64_t t, int32_t* d_err)
 {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     if (blockIdx.x == 0 && threadIdx.x == 0 && (row_off[0] != 0 || row_off[r] != nnz))
         set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(kBlock) k_csr_update(const int64_t* __restrict
                                                        const float* __restrict__ vals, int64_t r, int64_t c,
                                                        int64_t nnz, Op op, int32_t* d_err)
 {
+    pdl_enter();
     if (read_error(d_err)) return;
     const int lane = threadIdx.x & 31;
     const int64_t groups = (r + 31) / 32;
@@ -172,7 +174,7 @@ cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, in
                       cudaStream_t s)
 {
     SO_PROFILE("csr_check", s);
-    k_csr_check<<<group_blocks(r), kBlock, 0, s>>>(row_off, cols, r, c, nnz, full_rows, ls, ls_per_coord, t,
+    launch(k_csr_check, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, r, c, nnz, full_rows, ls, ls_per_coord, t,
                                                    d_err);
     return cudaGetLastError();
 }
@@ -181,7 +183,7 @@ cudaError_t csr_adam(const int64_t* row_off, const int32_t* cols, const float* v
                      int64_t nnz, const AdamParams& P, int32_t* d_err, cudaStream_t s)
 {
     SO_PROFILE("csr_update_adam", s);
-    k_csr_update<CsrAdamOp><<<group_blocks(r), kBlock, 0, s>>>(row_off, cols, vals, r, c, nnz,
+    launch(k_csr_update<CsrAdamOp>, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, vals, r, c, nnz,
                                                                CsrAdamOp{P, c}, d_err);
     return cudaGetLastError();
 }
@@ -190,7 +192,7 @@ cudaError_t csr_sgd(const int64_t* row_off, const int32_t* cols, const float* va
                     int64_t nnz, const SgdParams& P, int32_t* d_err, cudaStream_t s)
 {
     SO_PROFILE("csr_update_sgd", s);
-    k_csr_update<CsrSgdOp><<<group_blocks(r), kBlock, 0, s>>>(row_off, cols, vals, r, c, nnz,
+    launch(k_csr_update<CsrSgdOp>, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, vals, r, c, nnz,
                                                               CsrSgdOp{P, c}, d_err);
     return cudaGetLastError();
 }
@@ -200,6 +202,7 @@ __global__ void __launch_bounds__(kBlock) k_csr_to_coo(const int64_t* __restrict
                                                        const int32_t* __restrict__ cols, int64_t r, int64_t c,
                                                        int64_t nnz, int64_t* __restrict__ lin, int32_t* d_err)
 {
+    pdl_enter();
     if (read_error(d_err)) return;
     const int lane = threadIdx.x & 31;
     const int64_t groups = (r + 31) / 32;
@@ -221,7 +224,7 @@ cudaError_t csr_to_coo(const int64_t* row_off, const int32_t* cols, int64_t r, i
                        int64_t* lin_out, int32_t* d_err, cudaStream_t s)
 {
     SO_PROFILE("csr_to_coo", s);
-    k_csr_to_coo<<<group_blocks(r), kBlock, 0, s>>>(row_off, cols, r, c, nnz, lin_out, d_err);
+    launch(k_csr_to_coo, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, r, c, nnz, lin_out, d_err);
     return cudaGetLastError();
 }
 
@@ -229,6 +232,7 @@ cudaError_t csr_to_coo(const int64_t* row_off, const int32_t* cols, int64_t r, i
 __global__ void __launch_bounds__(kBlock) k_check_ascending(const int64_t* __restrict__ keys, int64_t n,
                                                             int64_t bound, int32_t* d_err)
 {
+    pdl_enter();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; i < n; i += stride) {
         const int64_t k = keys[i];
@@ -249,6 +253,7 @@ __global__ void __launch_bounds__(kBlock) k_merge_offsets(const int64_t* __restr
                                                           int64_t* __restrict__ row_off,
                                                           int32_t* __restrict__ cols, int32_t* d_err)
 {
+    pdl_enter();
     if (read_error(d_err)) return;
     const int64_t total = r + 1 + nb;
     const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x) * kMergeItems;
@@ -277,6 +282,7 @@ __global__ void __launch_bounds__(kBlock) k_merge_offsets(const int64_t* __restr
 __global__ void __launch_bounds__(kBlock) k_fill_cols(int32_t* __restrict__ cols, int64_t total, int64_t c,
                                                       int32_t* d_err)
 {
+    pdl_enter();
     if (read_error(d_err)) return;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; e < total; e += stride)
@@ -295,11 +301,11 @@ cudaError_t coo_to_csr(const int64_t* lin, int64_t nnz, int64_t r, int64_t c, in
     if (nnz > 0) {
         const int blocks = static_cast<int>(std::min<int64_t>(flat_blocks(nnz, 1), 8 * num_sms()));
         SO_PROFILE("check_ascending", s);
-        k_check_ascending<<<blocks, kBlock, 0, s>>>(lin, nnz, r * c, d_err);
+        launch(k_check_ascending, dim3(blocks), dim3(kBlock), s, lin, nnz, r * c, d_err);
     }
     SO_PROFILE("merge_offsets", s);
-    k_merge_offsets<<<flat_blocks(r + 1 + nnz, kMergeItems), kBlock, 0, s>>>(lin, nnz, r, c, 1, row_off_out,
-                                                                             cols_out, d_err);
+    launch(k_merge_offsets, dim3(flat_blocks(r + 1 + nnz, kMergeItems)), dim3(kBlock), s, lin, nnz, r, c, 1,
+           row_off_out, cols_out, d_err);
     return cudaGetLastError();
 }
 
@@ -309,17 +315,17 @@ cudaError_t row_coo_to_csr(const int64_t* rows, int64_t nrows, int64_t r, int64_
     if (nrows > 0) {
         const int blocks = static_cast<int>(std::min<int64_t>(flat_blocks(nrows, 1), 8 * num_sms()));
         SO_PROFILE("check_ascending", s);
-        k_check_ascending<<<blocks, kBlock, 0, s>>>(rows, nrows, r, d_err);
+        launch(k_check_ascending, dim3(blocks), dim3(kBlock), s, rows, nrows, r, d_err);
     }
     {
         SO_PROFILE("merge_offsets", s);
-        k_merge_offsets<<<flat_blocks(r + 1 + nrows, kMergeItems), kBlock, 0, s>>>(rows, nrows, r, 1, c,
-                                                                                   row_off_out, nullptr, d_err);
+        launch(k_merge_offsets, dim3(flat_blocks(r + 1 + nrows, kMergeItems)), dim3(kBlock), s, rows, nrows, r,
+               1, c, row_off_out, nullptr, d_err);
     }
     if (nrows > 0) {
         SO_PROFILE("fill_cols", s);
         const int blocks = static_cast<int>(std::min<int64_t>(flat_blocks(nrows * c, 4), 16 * num_sms()));
-        k_fill_cols<<<blocks, kBlock, 0, s>>>(cols_out, nrows * c, c, d_err);
+        launch(k_fill_cols, dim3(blocks), dim3(kBlock), s, cols_out, nrows * c, c, d_err);
     }
     return cudaGetLastError();
 }

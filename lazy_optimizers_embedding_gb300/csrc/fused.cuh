@@ -11,12 +11,11 @@
 // applied directly: the team loads the row's optimizer state and the piece's
 // gradient rows together, sums the gradient with error-free TwoSum
 // compensation, updates and stores.  A segment that spans several pieces (a
-// heavy Zipf head) is reduced by a deterministic tree: every piece writes a
-// compensated partial (sum, error) to a slot, and the last of each group of
-// kGroup pieces to arrive (atomic counter) combines the group's partials in
-// slot order; the last group combiner of the last level applies the update.
-// The order of every addition is fixed, so results are bit-reproducible, and
-// no thread ever waits on another.
+// heavy Zipf head) is reduced in two launches: the row kernel writes every
+// piece's compensated partial (sum, error) to a slot, then the combine kernel
+// merges each such segment's partials in piece order, one block per segment,
+// and applies the update.  The order of every addition is fixed, so results
+// are bit-reproducible, and no thread ever waits on another.
 //
 // Sum of duplicates per "DiskSparseAdam (DSA)" README, "Safe Duplicate
 // Aggregation"; update rules per "Module sparse_optimizer" (optirs-gpu 0.3.2
@@ -31,30 +30,38 @@
 
 namespace so {
 
-// Blocks of kBlock threads per SM the fused kernel is compiled for (4: at most
-// 64 registers, 32 warps per SM), gradient rows a lane requests at once when a
-// piece holds several entries (kRowIlp; twice that for pieces of split
-// segments), and single pieces a team takes per work ticket.  Overridable at
+// Blocks of kBlock threads per SM the row kernel is compiled for (3: at most 80
+// registers, 24 warps per SM), short pieces per work ticket (kTicket), gradient
+// rows a lane requests at once (kRowIlp), threads of a combine block and the
+// partial pairs a lane of it requests at once (kCombineIlp).  Overridable at
 // build time for tuning sweeps.
 #ifndef SO_FUSED_MIN_BLOCKS
-#define SO_FUSED_MIN_BLOCKS 4
+#define SO_FUSED_MIN_BLOCKS 3
+#endif
+#ifndef SO_TICKET
+#define SO_TICKET 4
 #endif
 #ifndef SO_ROW_ILP
 #define SO_ROW_ILP 4
 #endif
-#ifndef SO_TICKET_CHUNK
-#define SO_TICKET_CHUNK 4
+#ifndef SO_COMBINE_ILP
+#define SO_COMBINE_ILP 8
 #endif
 constexpr int kFusedMinBlocks = SO_FUSED_MIN_BLOCKS;
+constexpr int kTicket = SO_TICKET;
 constexpr int kRowIlp = SO_ROW_ILP;
-constexpr int kTicketChunk = SO_TICKET_CHUNK;
+constexpr int kCombineBlock = 128;
+constexpr int kGroup = 32;   // pieces merged by one team in the first combine stage
+constexpr int kCombineIlp = SO_COMBINE_ILP;
 
 struct PieceInfo {
     int64_t start, end;   // sorted positions [start, end)
     int64_t key;          // table row
     uint32_t u;           // segment index (row of a canonical output)
-    bool multi;           // segment spans several pieces
+    uint32_t flags;       // kMultiFlag: segment spans several pieces; kLongFlag: one long piece
     uint32_t perm0;       // input position of the first entry
+    __device__ __forceinline__ bool multi() const { return (flags & kMultiFlag) != 0u; }
+    __device__ __forceinline__ bool is_short() const { return flags == 0u; }
 };
 
 // Pieces of a raw input, from the sort and run detection.
@@ -63,10 +70,13 @@ struct SortedSrc {
     const uint32_t* sperm;
     const uint32_t* seg_off;
     const uint32_t* mlist;
+    const uint32_t* slist;
     const uint32_t* counts;
     __device__ __forceinline__ int64_t count() const { return counts[kCntP]; }
     __device__ __forceinline__ int64_t count_multi() const { return counts[kCntM]; }
     __device__ __forceinline__ int64_t multi_index(int64_t t) const { return mlist[t]; }
+    __device__ __forceinline__ int64_t count_split() const { return counts[kCntS]; }
+    __device__ __forceinline__ int64_t split_index(int64_t t) const { return slist[t]; }
     static constexpr bool kTickets = true;
     __device__ __forceinline__ uint32_t* ticket(int which) const { return const_cast<uint32_t*>(counts) + which; }
     __device__ __forceinline__ PieceInfo piece(int64_t j) const
@@ -78,12 +88,11 @@ struct SortedSrc {
         p.end = e;
         p.key = r.y;
         p.u = r.z & kSingleMask;
-        p.multi = (r.z & kMultiFlag) != 0u;
+        p.flags = r.z & (kMultiFlag | kLongFlag);
         p.perm0 = r.w;
         return p;
     }
     __device__ __forceinline__ uint32_t perm(int64_t e) const { return sperm[e]; }
-    __device__ __forceinline__ const uint32_t* perm_ptr(int64_t e) const { return sperm + e; }
     __device__ __forceinline__ void seg_bounds(uint32_t u, int64_t& s0, int64_t& s1) const
     {
         s0 = seg_off[u];
@@ -98,6 +107,8 @@ struct CanonSrc {
     __device__ __forceinline__ int64_t count() const { return n; }
     __device__ __forceinline__ int64_t count_multi() const { return 0; }
     __device__ __forceinline__ int64_t multi_index(int64_t) const { return 0; }
+    __device__ __forceinline__ int64_t count_split() const { return 0; }
+    __device__ __forceinline__ int64_t split_index(int64_t) const { return 0; }
     static constexpr bool kTickets = false;
     __device__ __forceinline__ uint32_t* ticket(int) const { return nullptr; }
     __device__ __forceinline__ PieceInfo piece(int64_t j) const
@@ -107,12 +118,11 @@ struct CanonSrc {
         p.end = j + 1;
         p.key = rows[j];
         p.u = static_cast<uint32_t>(j);
-        p.multi = false;
+        p.flags = 0u;
         p.perm0 = static_cast<uint32_t>(j);
         return p;
     }
     __device__ __forceinline__ uint32_t perm(int64_t e) const { return static_cast<uint32_t>(e); }
-    __device__ __forceinline__ const uint32_t* perm_ptr(int64_t) const { return nullptr; }   // never called: one entry per piece
     __device__ __forceinline__ void seg_bounds(uint32_t, int64_t& s0, int64_t& s1) const { s0 = s1 = 0; }
 };
 
@@ -238,6 +248,8 @@ __device__ __forceinline__ void sgd_coord(const SgdParams& P, float g, float& p,
 // read before the update (stage_last) and rewritten after it (end_row).
 struct AdamEpi {
     static constexpr const char* kName = "fused_rows_adam";
+    static constexpr const char* kCombineName = "combine_final_adam";
+    static constexpr const char* kGroupsName = "combine_groups_adam";
     static constexpr int kArrays = 3;   // p, m, v
     AdamParams P;
     int64_t c;
@@ -285,6 +297,8 @@ struct AdamEpi {
 
 struct SgdEpi {
     static constexpr const char* kName = "fused_rows_sgd";
+    static constexpr const char* kCombineName = "combine_final_sgd";
+    static constexpr const char* kGroupsName = "combine_groups_sgd";
     static constexpr int kArrays = 2;   // p, momentum buffer (absent without momentum)
     SgdParams P;
     int64_t c;
@@ -311,6 +325,8 @@ struct SgdEpi {
 // canonicalisation: write the summed row u
 struct StoreEpi {
     static constexpr const char* kName = "fused_rows_sum";
+    static constexpr const char* kCombineName = "combine_final_sum";
+    static constexpr const char* kGroupsName = "combine_groups_sum";
     static constexpr int kArrays = 1;   // no state; one dummy array keeps the types simple
     StoreParams P;
     int64_t c;
@@ -330,22 +346,29 @@ struct StoreEpi {
     __device__ __forceinline__ void end_row(const Row&, int, unsigned) const {}
 };
 
-// ------------------------------------------------------------ the kernel
+// ------------------------------------------------------------ the kernels
 // First gradient row of a piece at this lane's columns of the chunk at col0.
-// It initialises the sum (a lone value passes through bit for bit); the
-// compensation starts at -0.0 (s + -0.0 == s).
+// It initialises the sum: a lone value passes through bit for bit.
 template <int T, int NV, int V>
 __device__ __forceinline__ void first_row(const float* __restrict__ vals, int64_t c, int64_t col0, int tl,
-                                          uint32_t perm0, float (&s)[NV][V], float (&cm)[NV][V])
+                                          uint32_t perm0, float (&s)[NV][V])
 {
     const float* row = vals + static_cast<int64_t>(perm0) * c;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
         const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
         if (col < c) ld_grad<V>(row + col, s[k]);
+    }
+}
+
+// The TwoSum compensation of a sum starts at -0.0 (s + -0.0 == s).
+template <int NV, int V>
+__device__ __forceinline__ void zero_comp(float (&cm)[NV][V])
+{
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
 #pragma unroll
         for (int i = 0; i < V; ++i) cm[k][i] = -0.0f;
-    }
 }
 
 // Input positions of the entries after the first of a piece (fewer than
@@ -418,28 +441,24 @@ __device__ __forceinline__ void sum_rest(const Src& src, const PiecePerms<T>& pp
     }
 }
 
-// Pieces of a segment [s0, s1) and their partial-sum slots.  The first piece
-// starts at s0; piece i >= 1 starts at q1 + (i-1)*kPieceLen, where q1 is the
-// smallest multiple of kPieceLen >= s0 + kPieceLen (see run detection).  Piece
-// i >= 1 takes slot q1/kPieceLen + i - 1 (one per boundary position); the first
-// piece takes slot s0/kPieceLen when s0 is a multiple, else nb + s0/kPieceLen
-// (a split segment is longer than kPieceLen, so no two of them start in the same
-// block of kPieceLen positions).  2*nb slots in all.
-struct SlotMap {
-    int64_t q1b, first;
-    __device__ __forceinline__ SlotMap(int64_t s0, int64_t nb)
-        : q1b((s0 + 2 * kPieceLen - 1) / kPieceLen),
-          first((s0 % kPieceLen == 0) ? s0 / kPieceLen : nb + s0 / kPieceLen) {}
-    __device__ __forceinline__ int64_t operator()(int64_t i) const { return i == 0 ? first : q1b + i - 1; }
-    __device__ __forceinline__ int64_t pieces(int64_t s1) const
-    {
-        const int64_t q1 = q1b * kPieceLen;
-        return (s1 - 1 >= q1) ? 2 + (s1 - 1 - q1) / kPieceLen : 1;
-    }
-    __device__ __forceinline__ int64_t index(int64_t start, int64_t s0) const
-    {
-        return start == s0 ? 0 : start / kPieceLen - q1b + 1;
-    }
+// Pieces of a split segment [s0, s1) and their partial-sum slots.  The first
+// piece starts at s0; piece i >= 1 starts at q1 + (i-1)*kPieceLen, where q1 is
+// the smallest multiple of kPieceLen >= s0 + kPieceLen (see run detection).  A
+// piece starting at a multiple of kPieceLen takes slot start/kPieceLen; a first
+// piece starting elsewhere takes nb + start/kPieceLen (a split segment is
+// longer than kPieceLen, so no two of them start in the same block of kPieceLen
+// positions).  2*nb slots in all; a slot depends on the piece's start alone.
+__device__ __forceinline__ int64_t part_slot(int64_t start, int64_t nb)
+{
+    return (start % kPieceLen == 0) ? start / kPieceLen : nb + start / kPieceLen;
+}
+struct SplitSegment {
+    int64_t s0, s1, q1;
+    __device__ __forceinline__ SplitSegment(int64_t a, int64_t b)
+        : s0(a), s1(b), q1((a + 2 * kPieceLen - 1) / kPieceLen * kPieceLen) {}
+    __device__ __forceinline__ int64_t pieces() const { return (s1 - 1 >= q1) ? 2 + (s1 - 1 - q1) / kPieceLen : 1; }
+    __device__ __forceinline__ int64_t start(int64_t i) const { return i == 0 ? s0 : q1 + (i - 1) * kPieceLen; }
+    __device__ __forceinline__ int64_t index(int64_t st) const { return st == s0 ? 0 : (st - q1) / kPieceLen + 1; }
 };
 
 // Loads the optimizer state of one row chunk (the live arrays of the epilogue).
@@ -462,10 +481,34 @@ __device__ __forceinline__ void load_state(const Epi& epi, const PieceInfo& pc, 
     }
 }
 
-// Sums a piece's gradient rows and applies the update to its row (a piece that
-// holds its whole segment).  The row's state, last_step and first gradient row
-// are requested together, before any of them is used.
-template <int T, int NV, int V, class Src, class Epi>
+// Adds the rest of a piece's gradient rows (if any) to the first one, applies
+// the update to the row chunk at col0 and stores it.
+template <int T, int NV, int V, int ILP, class Src, class Epi>
+__device__ __forceinline__ void finish_chunk(const Src& src, const PiecePerms<T>& pp, const float* __restrict__ vals,
+                                             int64_t c, const Epi& epi, const PieceInfo& pc,
+                                             const typename Epi::Row& row, int64_t col0, int tl, unsigned tmask,
+                                             float (&x)[NV][Epi::kArrays][V], float (&s)[NV][V])
+{
+    if (pc.end - pc.start > 1) {
+        float cm[NV][V];
+        zero_comp<NV, V>(cm);
+        sum_rest<T, NV, V, ILP>(src, pp, vals, c, col0, tl, tmask, pc, s, cm);
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int i = 0; i < V; ++i) s[k][i] = __fadd_rn(s[k][i], cm[k][i]);
+    }
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+        if (col < c) epi.template apply<V>(row, col, x[k], s[k]);
+    }
+}
+
+// One piece holding its whole segment, row chunk by row chunk: the row's state,
+// last_step and first gradient row are requested together, the other gradient
+// rows ILP at a time.
+template <int T, int NV, int V, int ILP, class Src, class Epi>
 __device__ __forceinline__ void apply_single(const Src& src, const float* __restrict__ vals, int64_t c,
                                              const Epi& epi, const PieceInfo& pc, int tl, unsigned tmask)
 {
@@ -481,232 +524,338 @@ __device__ __forceinline__ void apply_single(const Src& src, const float* __rest
         float x[NV][A][V];
         load_state<T, NV, V>(epi, pc, c, col0, tl, x);
         if (cc == 0 && lp) last = *lp;
-        float s[NV][V], cm[NV][V];
-        first_row<T, NV, V>(vals, c, col0, tl, pc.perm0, s, cm);
-        if (pc.end - pc.start > 1) sum_rest<T, NV, V, kRowIlp>(src, pp, vals, c, col0, tl, tmask, pc, s, cm);
-        const typename Epi::Row row = epi.make_row(pc, last);
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-            if (col < c) {
-                float g[V];
-#pragma unroll
-                for (int i = 0; i < V; ++i) g[i] = __fadd_rn(s[k][i], cm[k][i]);
-                epi.template apply<V>(row, col, x[k], g);
-            }
-        }
+        float s[NV][V];
+        first_row<T, NV, V>(vals, c, col0, tl, pc.perm0, s);
+        finish_chunk<T, NV, V, ILP>(src, pp, vals, c, epi, pc, epi.make_row(pc, last), col0, tl, tmask, x, s);
     }
     epi.end_row(epi.make_row(pc, last), tl, tmask);
 }
 
-// A piece of a multi-piece segment: its compensated partial sum goes to its
-// level-0 slot; then, level by level, the team bumps its group's counter and
-// only the last of the group to arrive continues: it sums the group's partials
-// in slot order into the slot of the group's first member (whose partial it has
-// just consumed), and at the top level applies the update instead.  The order
-// of every addition is fixed by the slots, whichever team arrives last.  Out of
-// line: it runs for few pieces, and its registers stay out of the budget of the
-// single-piece path.
-template <int T, int NV, int V, class Src, class Epi>
-__device__ __noinline__ void apply_multi(const Src& src, const float* __restrict__ vals, int64_t c,
-                                            const Epi& epi, float* __restrict__ part,
-                                            uint32_t* __restrict__ lvl_cnt, int64_t nb, const PieceInfo pc,
-                                            int tl, unsigned tmask)
+// Lane `from` of the team's piece, for every lane of the team.
+template <int T>
+__device__ __forceinline__ PieceInfo shfl_piece(const PieceInfo& p, int from, unsigned tmask)
+{
+    PieceInfo q;
+    q.start = __shfl_sync(tmask, static_cast<long long>(p.start), from, T);
+    q.end = __shfl_sync(tmask, static_cast<long long>(p.end), from, T);
+    q.key = __shfl_sync(tmask, static_cast<long long>(p.key), from, T);
+    q.u = __shfl_sync(tmask, p.u, from, T);
+    q.flags = __shfl_sync(tmask, p.flags, from, T);
+    q.perm0 = __shfl_sync(tmask, p.perm0, from, T);
+    return q;
+}
+
+// A piece of a split segment: its compensated partial sum (sum, error) goes to
+// the piece's slot, to be combined by k_combine_split.
+template <int T, int NV, int V, class Src>
+__device__ __forceinline__ void store_partial(const Src& src, const float* __restrict__ vals, int64_t c,
+                                              float* __restrict__ part, int64_t nb, const PieceInfo& pc, int tl,
+                                              unsigned tmask)
 {
     constexpr int CW = T * NV * V;
-    constexpr int A = Epi::kArrays;
     const int nchunks = static_cast<int>((c + CW - 1) / CW);
-    const int64_t nslots = 2 * nb;
-    int64_t s0, s1;
-    src.seg_bounds(pc.u, s0, s1);
-    const SlotMap slot_of(s0, nb);
-    int64_t Kl = slot_of.pieces(s1);          // items at this level
-    int64_t kl = slot_of.index(pc.start, s0);
-    {
-        float* ps = part + slot_of(kl) * 2 * c;
-        PiecePerms<T> pp;
-        pp.load(src, pc, tl);
-        for (int cc = 0; cc < nchunks; ++cc) {
-            const int64_t col0 = static_cast<int64_t>(cc) * CW;
-            float s[NV][V], cm[NV][V];
-            first_row<T, NV, V>(vals, c, col0, tl, pc.perm0, s, cm);
-            sum_rest<T, NV, V, 2 * kRowIlp>(src, pp, vals, c, col0, tl, tmask, pc, s, cm);
+    float* ps = part + part_slot(pc.start, nb) * 2 * c;
+    PiecePerms<T> pp;
+    pp.load(src, pc, tl);
+    for (int cc = 0; cc < nchunks; ++cc) {
+        const int64_t col0 = static_cast<int64_t>(cc) * CW;
+        float s[NV][V], cm[NV][V];
+        first_row<T, NV, V>(vals, c, col0, tl, pc.perm0, s);
+        zero_comp<NV, V>(cm);
+        sum_rest<T, NV, V, kRowIlp>(src, pp, vals, c, col0, tl, tmask, pc, s, cm);
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                if (col < c) {
-                    st_part<V>(ps + col, s[k]);
-                    st_part<V>(ps + c + col, cm[k]);
-                }
+        for (int k = 0; k < NV; ++k) {
+            const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+            if (col < c) {
+                st_part<V>(ps + col, s[k]);
+                st_part<V>(ps + c + col, cm[k]);
             }
         }
-    }
-    int64_t stride = 1;                        // level-0 pieces per item of this level
-    for (int lvl = 0;; ++lvl) {
-        __threadfence();
-        __syncwarp(tmask);
-        const int64_t g = kl / kGroup;
-        const int64_t members = (Kl - g * kGroup) < kGroup ? (Kl - g * kGroup) : kGroup;
-        const int64_t lead_slot = slot_of(g * kGroup * stride);
-        uint32_t old = 0;
-        if (tl == 0) old = atomicAdd(lvl_cnt + lvl * nslots + lead_slot, 1u);
-        old = __shfl_sync(tmask, old, 0, T);
-        if (static_cast<int64_t>(old) != members - 1) return;   // not the last of its group
-        __threadfence();
-        const int64_t Knext = (Kl + kGroup - 1) / kGroup;
-        const bool final = (Knext == 1);
-        const int64_t* lp = final ? epi.stage_last(pc) : nullptr;
-        const int64_t last = lp ? *lp : 0;
-        for (int cc = 0; cc < nchunks; ++cc) {
-            const int64_t col0 = static_cast<int64_t>(cc) * CW;
-            float S[NV][V], C[NV][V];
-            constexpr int MR = NV >= 4 ? 1 : 4 / NV;   // partials requested at once
-            for (int64_t m0 = 0; m0 < members; m0 += MR) {
-                float xs[MR][NV][V], xc[MR][NV][V];
-#pragma unroll
-                for (int r = 0; r < MR; ++r) {
-                    if (m0 + r < members) {
-                        const float* ps = part + (slot_of((g * kGroup + m0 + r) * stride) * 2) * c;
-#pragma unroll
-                        for (int k = 0; k < NV; ++k) {
-                            const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                            if (col < c) {
-                                ld_part<V>(ps + col, xs[r][k]);
-                                ld_part<V>(ps + c + col, xc[r][k]);
-                            }
-                        }
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < MR; ++r) {
-                    if (m0 + r < members) {
-#pragma unroll
-                        for (int k = 0; k < NV; ++k)
-#pragma unroll
-                            for (int i = 0; i < V; ++i) {
-                                if (m0 + r == 0) {
-                                    S[k][i] = xs[r][k][i];
-                                    C[k][i] = xc[r][k][i];
-                                } else {
-                                    two_sum_merge(S[k][i], C[k][i], xs[r][k][i], xc[r][k][i]);
-                                }
-                            }
-                    }
-                }
-            }
-            if (final) {
-                float x[NV][A][V];
-                load_state<T, NV, V>(epi, pc, c, col0, tl, x);
-                const typename Epi::Row row = epi.make_row(pc, last);
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                    if (col < c) {
-                        float gsum[V];
-#pragma unroll
-                        for (int i = 0; i < V; ++i) gsum[i] = __fadd_rn(S[k][i], C[k][i]);
-                        epi.template apply<V>(row, col, x[k], gsum);
-                    }
-                }
-            } else {
-                float* pd = part + (lead_slot * 2) * c;
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                    if (col < c) {
-                        st_part<V>(pd + col, S[k]);
-                        st_part<V>(pd + c + col, C[k]);
-                    }
-                }
-            }
-        }
-        if (final) {
-            epi.end_row(epi.make_row(pc, last), tl, tmask);
-            return;
-        }
-        kl = g;
-        Kl = Knext;
-        stride *= kGroup;
     }
 }
 
-// Teams first take the pieces of multi-piece segments (from the list run
-// detection built, so these longer dependency chains start first and overlap
-// the other teams' streaming), then the single pieces.  Work is handed out by
-// atomic tickets on a raw input, statically on a canonical one.
+// Every piece of the input.  On a raw input the pieces range from one to
+// 2*kPieceLen-1 gradient rows, so they are handed out by atomic tickets, long
+// pieces first (the list run detection built: pieces of split segments, whose
+// partials the combine kernel waits for, and whole segments of more than
+// kShortLen entries), one per ticket, then short pieces kTicket per ticket
+// (their records one per lane).  A team requests its next ticket and that
+// ticket's records while it works on the current ones.  A canonical input (one
+// row per piece) is split statically, each team fetching the record of its
+// next piece during the current one.
 template <int T, int NV, int V, class Src, class Epi>
 __global__ void __launch_bounds__(kBlock, kFusedMinBlocks) k_fused_rows(Src src, const float* __restrict__ vals,
                                                                         int64_t c, Epi epi, float* __restrict__ part,
-                                                                        uint32_t* __restrict__ lvl_cnt, int64_t nb,
-                                                                        int32_t* d_err)
+                                                                        int64_t nb, int32_t* d_err)
 {
+    pdl_enter();
     if (read_error(d_err)) return;
     constexpr int kTeams = kBlock / T;
     const int lane = threadIdx.x & 31;
     const int tl = lane & (T - 1);
     const unsigned tmask = (T == 32) ? kFull : (((1u << T) - 1u) << (lane & ~(T - 1)));
-    const int64_t team_g = static_cast<int64_t>(blockIdx.x) * kTeams + threadIdx.x / T;
-    const int64_t nteams = static_cast<int64_t>(gridDim.x) * kTeams;
     const int64_t P = src.count();
     if constexpr (Src::kTickets) {
-        // dynamic: multi pieces one per ticket until they run out, then single
-        // pieces kTicketChunk per ticket, so teams held up by a multi piece take
-        // fewer single pieces
-        const int64_t M = src.count_multi();
-        while (true) {
+        const auto take = [&](int which) {
             uint32_t t = 0;
-            if (tl == 0) t = atomicAdd(src.ticket(kTicketM), 1u);
-            t = __shfl_sync(tmask, t, 0, T);
-            if (t >= M) break;
-            apply_multi<T, NV, V>(src, vals, c, epi, part, lvl_cnt, nb, src.piece(src.multi_index(t)), tl, tmask);
+            if (tl == 0) t = atomicAdd(src.ticket(which), 1u);
+            return t;
+        };
+        {   // long pieces
+            const int64_t M = src.count_multi();
+            const auto record = [&](uint32_t t, PieceInfo& r) {
+                if (tl == 0 && t < M) r = src.piece(src.multi_index(t));
+            };
+            uint32_t ta = __shfl_sync(tmask, take(kTicketM), 0, T);
+            uint32_t tb = take(kTicketM);
+            PieceInfo ra{}, rb{};
+            record(ta, ra);
+            tb = __shfl_sync(tmask, tb, 0, T);
+            while (ta < M) {
+                record(tb, rb);
+                const uint32_t tc = (tb < M) ? take(kTicketM) : tb;
+                const PieceInfo pc = shfl_piece<T>(ra, 0, tmask);
+                if (pc.multi())
+                    store_partial<T, NV, V>(src, vals, c, part, nb, pc, tl, tmask);
+                else
+                    apply_single<T, NV, V, kRowIlp>(src, vals, c, epi, pc, tl, tmask);
+                ta = tb;
+                ra = rb;
+                tb = __shfl_sync(tmask, tc, 0, T);
+            }
         }
-        while (true) {
-            uint32_t t = 0;
-            if (tl == 0) t = atomicAdd(src.ticket(kTicketS), 1u);
-            t = __shfl_sync(tmask, t, 0, T);
-            const int64_t j0 = static_cast<int64_t>(t) * kTicketChunk;
-            if (j0 >= P) break;
-            const int64_t j1 = (j0 + kTicketChunk) < P ? j0 + kTicketChunk : P;
-            for (int64_t j = j0; j < j1; ++j) {
-                const PieceInfo pc = src.piece(j);
-                if (!pc.multi) apply_single<T, NV, V>(src, vals, c, epi, pc, tl, tmask);
+        {   // short pieces
+            constexpr int K = kTicket < T ? kTicket : T;
+            const int64_t nt = (P + K - 1) / K;
+            const auto records = [&](uint32_t t, PieceInfo& r) {
+                const int64_t j = static_cast<int64_t>(t) * K + tl;
+                if (tl < K && j < P) r = src.piece(j);
+            };
+            uint32_t ta = __shfl_sync(tmask, take(kTicketS), 0, T);
+            uint32_t tb = take(kTicketS);
+            PieceInfo ra{}, rb{};
+            records(ta, ra);
+            tb = __shfl_sync(tmask, tb, 0, T);
+            while (ta < nt) {
+                records(tb, rb);
+                const uint32_t tc = (tb < nt) ? take(kTicketS) : tb;
+                const int64_t j0 = static_cast<int64_t>(ta) * K;
+                const int nd = (P - j0) < K ? static_cast<int>(P - j0) : K;
+                for (int d = 0; d < nd; ++d) {
+                    const PieceInfo pc = shfl_piece<T>(ra, d, tmask);
+                    if (pc.is_short()) apply_single<T, NV, V, kRowIlp>(src, vals, c, epi, pc, tl, tmask);
+                }
+                ta = tb;
+                ra = rb;
+                tb = __shfl_sync(tmask, tc, 0, T);
             }
         }
     } else {
-        (void)nteams;
-        for (int64_t j = team_g; j < P; j += nteams)
-            apply_single<T, NV, V>(src, vals, c, epi, src.piece(j), tl, tmask);
+        const int64_t team_g = static_cast<int64_t>(blockIdx.x) * kTeams + threadIdx.x / T;
+        const int64_t nteams = static_cast<int64_t>(gridDim.x) * kTeams;
+        PieceInfo mine{};
+        if (team_g < P && tl == 0) mine = src.piece(team_g);
+        for (int64_t j = team_g; j < P; j += nteams) {
+            const PieceInfo pc = shfl_piece<T>(mine, 0, tmask);
+            if (j + nteams < P && tl == 0) mine = src.piece(j + nteams);
+            apply_single<T, NV, V, kRowIlp>(src, vals, c, epi, pc, tl, tmask);
+        }
+    }
+}
+
+// Merges the partial pairs of pieces i0, i0 + step, ... (cnt of them) of a split
+// segment, in that order, at this lane's columns of the chunk at col0.
+template <int T, int NV, int V>
+__device__ __forceinline__ void merge_partials(const float* __restrict__ part, int64_t c, int64_t nb,
+                                               const SplitSegment& seg, int64_t i0, int64_t step, int64_t cnt,
+                                               int64_t col0, int tl, float (&S)[NV][V], float (&C)[NV][V])
+{
+    constexpr int MR = NV >= kCombineIlp ? 1 : kCombineIlp / NV;   // partial pairs requested at once
+    for (int64_t m0 = 0; m0 < cnt; m0 += MR) {
+        float xs[MR][NV][V], xc[MR][NV][V];
+#pragma unroll
+        for (int r = 0; r < MR; ++r) {
+            if (m0 + r < cnt) {
+                const float* ps = part + part_slot(seg.start(i0 + (m0 + r) * step), nb) * 2 * c;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+                    if (col < c) {
+                        ld_part<V>(ps + col, xs[r][k]);
+                        ld_part<V>(ps + c + col, xc[r][k]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < MR; ++r) {
+            if (m0 + r < cnt) {
+#pragma unroll
+                for (int k = 0; k < NV; ++k)
+#pragma unroll
+                    for (int i = 0; i < V; ++i) {
+                        if (m0 + r == 0) {
+                            S[k][i] = xs[r][k][i];
+                            C[k][i] = xc[r][k][i];
+                        } else {
+                            two_sum_merge(S[k][i], C[k][i], xs[r][k][i], xc[r][k][i]);
+                        }
+                    }
+            }
+        }
+    }
+}
+
+// First combine stage: the pieces of every split segment in groups of kGroup
+// consecutive pieces (one team per group, found through its first piece, whose
+// slot receives the group's merged pair: the team has consumed that partial).
+template <int T, int NV, int V, class Src>
+__global__ void __launch_bounds__(kCombineBlock) k_combine_groups(Src src, int64_t c, float* __restrict__ part,
+                                                                  int64_t nb, int32_t* d_err)
+{
+    pdl_enter();
+    if (read_error(d_err)) return;
+    constexpr int kTeams = kCombineBlock / T;
+    constexpr int CW = T * NV * V;
+    const int lane = threadIdx.x & 31;
+    const int tl = lane & (T - 1);
+    const int64_t team_g = static_cast<int64_t>(blockIdx.x) * kTeams + threadIdx.x / T;
+    const int64_t nteams = static_cast<int64_t>(gridDim.x) * kTeams;
+    const int nchunks = static_cast<int>((c + CW - 1) / CW);
+    const int64_t M = src.count_multi();
+    for (int64_t t = team_g; t < M; t += nteams) {
+        const PieceInfo pc = src.piece(src.multi_index(t));
+        if (!pc.multi()) continue;
+        int64_t s0, s1;
+        src.seg_bounds(pc.u, s0, s1);
+        const SplitSegment seg(s0, s1);
+        const int64_t i = seg.index(pc.start);
+        if (i % kGroup != 0) continue;
+        const int64_t K = seg.pieces();
+        const int64_t cnt = (K - i) < kGroup ? (K - i) : kGroup;
+        if (cnt < 2) continue;
+        float* pd = part + part_slot(pc.start, nb) * 2 * c;
+        for (int cc = 0; cc < nchunks; ++cc) {
+            const int64_t col0 = static_cast<int64_t>(cc) * CW;
+            float S[NV][V], C[NV][V];
+            merge_partials<T, NV, V>(part, c, nb, seg, i, 1, cnt, col0, tl, S, C);
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+                if (col < c) {
+                    st_part<V>(pd + col, S[k]);
+                    st_part<V>(pd + c + col, C[k]);
+                }
+            }
+        }
+    }
+}
+
+// Second combine stage: one team per split segment merges its groups' pairs in
+// group order and applies the update.
+template <int T, int NV, int V, class Src, class Epi>
+__global__ void __launch_bounds__(kCombineBlock) k_combine_final(Src src, int64_t c, Epi epi,
+                                                                 const float* __restrict__ part, int64_t nb,
+                                                                 int32_t* d_err)
+{
+    pdl_enter();
+    if (read_error(d_err)) return;
+    constexpr int kTeams = kCombineBlock / T;
+    constexpr int CW = T * NV * V;
+    constexpr int A = Epi::kArrays;
+    const int lane = threadIdx.x & 31;
+    const int tl = lane & (T - 1);
+    const unsigned tmask = (T == 32) ? kFull : (((1u << T) - 1u) << (lane & ~(T - 1)));
+    const int64_t team_g = static_cast<int64_t>(blockIdx.x) * kTeams + threadIdx.x / T;
+    const int64_t nteams = static_cast<int64_t>(gridDim.x) * kTeams;
+    const int nchunks = static_cast<int>((c + CW - 1) / CW);
+    const int64_t S_ = src.count_split();
+    for (int64_t t = team_g; t < S_; t += nteams) {
+        const PieceInfo pc = src.piece(src.split_index(t));   // the segment's first piece
+        int64_t s0, s1;
+        src.seg_bounds(pc.u, s0, s1);
+        const SplitSegment seg(s0, s1);
+        const int64_t ng = (seg.pieces() + kGroup - 1) / kGroup;
+        const int64_t* lp = epi.stage_last(pc);
+        const int64_t last = lp ? *lp : 0;
+        const typename Epi::Row row = epi.make_row(pc, last);
+        for (int cc = 0; cc < nchunks; ++cc) {
+            const int64_t col0 = static_cast<int64_t>(cc) * CW;
+            float x[NV][A][V];
+            load_state<T, NV, V>(epi, pc, c, col0, tl, x);
+            float S[NV][V], C[NV][V];
+            merge_partials<T, NV, V>(part, c, nb, seg, 0, kGroup, ng, col0, tl, S, C);
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+                if (col < c) {
+                    float g[V];
+#pragma unroll
+                    for (int i = 0; i < V; ++i) g[i] = __fadd_rn(S[k][i], C[k][i]);
+                    epi.template apply<V>(row, col, x[k], g);
+                }
+            }
+        }
+        epi.end_row(row, tl, tmask);
     }
 }
 
 // ------------------------------------------------------------ launch
-template <int T, int NV, int V, class Src, class Epi>
-cudaError_t launch_shape(const Src& src, int64_t max_pieces, const float* vals, int64_t c, const Epi& epi,
-                         float* part, uint32_t* lvl_cnt, int64_t nb, int32_t* d_err, cudaStream_t s)
+template <class K>
+int max_blocks(K kernel, int threads)
 {
-    static int occ = 0;
-    if (occ == 0) {
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_fused_rows<T, NV, V, Src, Epi>, kBlock, 0);
-        if (occ <= 0) occ = 1;
-    }
+    int occ = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0);
+    return occ > 0 ? occ : 1;
+}
+
+// The row kernel, then (on a raw input that may hold split segments) the
+// combine kernel.  max_split bounds the number of split segments (0: none).
+template <int T, int NV, int V, class Src, class Epi>
+cudaError_t launch_shape(const Src& src, int64_t max_pieces, int64_t max_split, const float* vals, int64_t c,
+                         const Epi& epi, float* part, int64_t nb, int32_t* d_err, cudaStream_t s)
+{
     constexpr int kTeams = kBlock / T;
-    const int64_t want = (max_pieces + kTeams - 1) / kTeams;
-    const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)occ * num_sms())));
-    SO_PROFILE(Epi::kName, s);
-    k_fused_rows<T, NV, V, Src, Epi><<<blocks, kBlock, 0, s>>>(src, vals, c, epi, part, lvl_cnt, nb, d_err);
-    return cudaGetLastError();
+    {
+        static const int occ = max_blocks(k_fused_rows<T, NV, V, Src, Epi>, kBlock);
+        const int64_t cap = static_cast<int64_t>(occ) * num_sms();
+        const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cap, (max_pieces + kTeams - 1) / kTeams)));
+        SO_PROFILE(Epi::kName, s);
+        launch(k_fused_rows<T, NV, V, Src, Epi>, dim3(blocks), dim3(kBlock), s, src, vals, c, epi, part, nb, d_err);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (max_split > 0) {
+        constexpr int kCTeams = kCombineBlock / T;
+        static const int occ = max_blocks(k_combine_groups<T, NV, V, Src>, kCombineBlock);
+        const int64_t cap = static_cast<int64_t>(occ) * num_sms();
+        {
+            SO_PROFILE(Epi::kGroupsName, s);
+            const int64_t gb = std::min<int64_t>(cap, (2 * nb + kCTeams - 1) / kCTeams);
+            launch(k_combine_groups<T, NV, V, Src>, dim3(static_cast<unsigned>(gb)), dim3(kCombineBlock), s, src, c, part, nb,
+                                                                                               d_err);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        SO_PROFILE(Epi::kCombineName, s);
+        const int64_t fb = std::min<int64_t>(cap, (max_split + kCTeams - 1) / kCTeams);
+        launch(k_combine_final<T, NV, V, Src, Epi>, dim3(static_cast<unsigned>(fb)), dim3(kCombineBlock), s, src, c, epi, part, nb,
+                                                                                             d_err);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
 }
 
 // Team shape: smallest power-of-two team that covers a row with one vector per
 // lane; rows wider than 32 vectors give each lane 2 vectors per chunk and are
 // walked in chunks of 256 (or 128 scalar) columns.
 template <class Src, class Epi>
-cudaError_t launch_fused(const Src& src, int64_t max_pieces, const float* vals, int64_t c, const Epi& epi,
-                         float* part, uint32_t* lvl_cnt, int64_t nb, int vec4, int32_t* d_err,
-                         cudaStream_t s)
+cudaError_t launch_fused(const Src& src, int64_t max_pieces, int64_t max_split, const float* vals, int64_t c,
+                         const Epi& epi, float* part, int64_t nb, int vec4, int32_t* d_err, cudaStream_t s)
 {
     if (max_pieces <= 0) return cudaSuccess;
-#define SO_LAUNCH(T, NV, V) launch_shape<T, NV, V>(src, max_pieces, vals, c, epi, part, lvl_cnt, nb, d_err, s)
+#define SO_LAUNCH(T, NV, V) \
+    launch_shape<T, NV, V>(src, max_pieces, max_split, vals, c, epi, part, nb, d_err, s)
     if (vec4) {
         const int64_t nv = c / 4;
         if (nv <= 1) return SO_LAUNCH(1, 1, 4);
@@ -729,7 +878,7 @@ cudaError_t launch_fused(const Src& src, int64_t max_pieces, const float* vals, 
 
 inline SortedSrc sorted_src(const SortWs& ws)
 {
-    return SortedSrc{ws.rec, ws.vals[ws.final_buf], ws.seg_off, ws.mlist, ws.counts};
+    return SortedSrc{ws.rec, ws.vals[ws.final_buf], ws.seg_off, ws.mlist, ws.slist, ws.counts};
 }
 
 }  // namespace so

@@ -8,14 +8,14 @@ namespace so {
 cudaError_t fused_rows_adam_sorted(const SortWs& ws, const WsLayout& L, const float* vals, int64_t c,
                                    const AdamParams& P, int vec4, int32_t* d_err, cudaStream_t s)
 {
-    return launch_fused(sorted_src(ws), L.n + L.nb, vals, c, AdamEpi{P, c}, ws.part, ws.lvl_cnt, L.nb,
+    return launch_fused(sorted_src(ws), L.n, L.n > kPieceLen ? L.nb : 0, vals, c, AdamEpi{P, c}, ws.part, L.nb,
                         vec4, d_err, s);
 }
 
 cudaError_t fused_rows_adam_canon(const int64_t* rows, int64_t n, const float* vals, int64_t c,
                                   const AdamParams& P, int vec4, int32_t* d_err, cudaStream_t s)
 {
-    return launch_fused(CanonSrc{rows, n}, n, vals, c, AdamEpi{P, c}, nullptr, nullptr, 0, vec4, d_err, s);
+    return launch_fused(CanonSrc{rows, n}, n, 0, vals, c, AdamEpi{P, c}, nullptr, 0, vec4, d_err, s);
 }
 
 }  // namespace so

@@ -49,9 +49,6 @@ WsLayout ws_layout(int64_t n, int64_t c, int64_t bound)
     L.passes = (key_bits(bound) + 7) / 8;
     L.sort_tiles = (int)((n + kSortTile - 1) / kSortTile);
     L.run_tiles = (int)((n + kRunTile - 1) / kRunTile);
-    int levels = 1;
-    for (int64_t k = L.nb + 1; k > 1; k = (k + kGroup - 1) / kGroup) ++levels;
-    L.levels = levels;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         off = align_up(off, 256);
@@ -66,14 +63,15 @@ WsLayout ws_layout(int64_t n, int64_t c, int64_t bound)
     L.rec = take(sizeof(uint4) * (size_t)(n + L.nb + 2));
     L.seg_off = take(sizeof(uint32_t) * (size_t)(n + 1));
     L.mlist = take(sizeof(uint32_t) * (size_t)(n + L.nb + 2));
+    L.slist = take(sizeof(uint32_t) * (size_t)(L.nb + 1));
     L.part = take(sizeof(float) * (size_t)(2 * L.nb) * 2 * (size_t)c);
+    L.hist_blocks = (int)std::min<int64_t>((n + kBlock * kHistItems - 1) / (kBlock * kHistItems), kMaxHistBlocks);
+    L.bh = take(sizeof(uint32_t) * (size_t)L.hist_blocks * kMaxPasses * 256);
     off = align_up(off, 256);
     L.ctrl_begin = off;
-    L.gh = take(sizeof(uint32_t) * kMaxPasses * 256);
     L.counts = take(sizeof(uint32_t) * kCountsWords);
     L.rstatus = take(sizeof(uint32_t) * (size_t)L.passes * L.sort_tiles * 256);
     L.dstatus = take(sizeof(unsigned long long) * (size_t)L.run_tiles);
-    L.lvl_cnt = take(sizeof(uint32_t) * (size_t)L.levels * 2 * L.nb);
     L.ctrl_end = align_up(off, 256);
     L.total = L.ctrl_end;
     return L;
@@ -90,30 +88,35 @@ SortWs carve(const WsLayout& L, void* ws)
     w.rec = reinterpret_cast<uint4*>(b + L.rec);
     w.seg_off = reinterpret_cast<uint32_t*>(b + L.seg_off);
     w.mlist = reinterpret_cast<uint32_t*>(b + L.mlist);
+    w.slist = reinterpret_cast<uint32_t*>(b + L.slist);
     w.part = reinterpret_cast<float*>(b + L.part);
-    w.gh = reinterpret_cast<uint32_t*>(b + L.gh);
+    w.bh = reinterpret_cast<uint32_t*>(b + L.bh);
     w.counts = reinterpret_cast<uint32_t*>(b + L.counts);
     w.rstatus = reinterpret_cast<uint32_t*>(b + L.rstatus);
     w.dstatus = reinterpret_cast<unsigned long long*>(b + L.dstatus);
-    w.lvl_cnt = reinterpret_cast<uint32_t*>(b + L.lvl_cnt);
     w.final_buf = (L.passes - 1) & 1;
     return w;
 }
 
 // ---------------------------------------------------------------------- K1
-// Range check (0 <= idx < bound) and the digit histograms of all passes.  Every
-// key is counted, valid or not, with the same truncation the radix passes use,
-// so the scatter offsets stay inside [0, n) whatever the input.  Each thread
-// requests its kHistItems keys at once (128-bit loads when aligned), then
-// counts them in shared memory; one global atomic per non-empty bin and block.
-constexpr int kHistItems = 8;
-
+// Range check (0 <= idx < bound) and the digit histograms of all passes, one
+// set per block (bh[block][pass][digit], read by every radix tile), so nothing
+// has to be zeroed before this kernel: it zeroes the control words the later
+// kernels of the call count in (ctrl, 16-byte words).  Every key is counted,
+// valid or not, with the same truncation the radix passes use, so the scatter
+// offsets stay inside [0, n) whatever the input.  Each thread requests its
+// kHistItems keys at once (128-bit loads when aligned), then counts them in
+// shared memory.
 __global__ void __launch_bounds__(kBlock) k_range_hist(const int64_t* __restrict__ idx, uint32_t n,
-                                                       int64_t bound, int passes,
-                                                       uint32_t* __restrict__ gh, int32_t* d_err)
+                                                       int64_t bound, int passes, uint32_t* __restrict__ bh,
+                                                       uint4* __restrict__ ctrl, uint32_t ctrl_words,
+                                                       int32_t* d_err)
 {
+    pdl_enter();
     __shared__ uint32_t sh[kMaxPasses * 256];
     for (int i = threadIdx.x; i < kMaxPasses * 256; i += kBlock) sh[i] = 0;
+    for (uint32_t i = blockIdx.x * kBlock + threadIdx.x; i < ctrl_words; i += gridDim.x * kBlock)
+        ctrl[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     int bad = 0;
     const uint32_t stride = gridDim.x * kBlock * kHistItems;
@@ -140,10 +143,8 @@ __global__ void __launch_bounds__(kBlock) k_range_hist(const int64_t* __restrict
         }
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) set_error(d_err, SPARSE_ERR_INDEX_OUT_OF_RANGE);
-    for (int i = threadIdx.x; i < passes * 256; i += kBlock) {
-        const uint32_t v = sh[i];
-        if (v) atomicAdd(gh + i, v);
-    }
+    uint32_t* mine = bh + static_cast<size_t>(blockIdx.x) * kMaxPasses * 256;
+    for (int i = threadIdx.x; i < passes * 256; i += kBlock) mine[i] = sh[i];
 }
 
 // ---------------------------------------------------------------------- K2
@@ -163,10 +164,11 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
                                                        const uint32_t* __restrict__ vin,
                                                        uint32_t* __restrict__ kout,
                                                        uint32_t* __restrict__ vout, uint32_t n, int shift,
-                                                       const uint32_t* __restrict__ gh,
+                                                       const uint32_t* __restrict__ bh, int hist_blocks,
                                                        uint32_t* status, uint32_t* tile_ctr,
                                                        int32_t* d_err)
 {
+    pdl_enter();
     constexpr int kWarps = kBlock / 32;
     __shared__ uint32_t s_wh[kWarps][256];
     __shared__ uint32_t s_gbase[256];
@@ -235,7 +237,16 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
 
     uint32_t total;
     s_texcl[tid] = block_excl_scan(tcount, s_scan, &total);
-    const uint32_t gexcl = block_excl_scan(gh[tid], s_scan, &total);
+    uint32_t gcount = 0;   // digit tid over the whole input: the blocks' histograms of this pass
+    for (int b0 = 0; b0 < hist_blocks; b0 += 8) {
+        uint32_t h[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            h[q] = (b0 + q < hist_blocks) ? bh[static_cast<size_t>(b0 + q) * kMaxPasses * 256 + tid] : 0u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) gcount += h[q];
+    }
+    const uint32_t gexcl = block_excl_scan(gcount, s_scan, &total);
 
     // look-back: kLook predecessor words per round trip, consumed nearest first
     // until an inclusive one; a word not yet published stops the round (its
@@ -307,21 +318,25 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
 // kPieceLen.  Outputs (u = segment index,
 // j = piece index):
 //   seg_off[u] = first sorted position of segment u, seg_off[U] = n
-//   rec[j] = {start, key, u | kMultiFlag if the segment spans several pieces,
+//   rec[j] = {start, key, u | kMultiFlag if the segment spans several pieces
+//             | kLongFlag if it is one piece of more than kShortLen entries,
 //             input position of the start}, rec[P] = {n, 0, 0, 0}
-//   mlist[0 .. M) = the indices j of the multi-piece pieces, in no particular
-//             order (appended through an atomic counter; the order in which
-//             they are processed does not affect any result)
+//   mlist[0 .. M) = the indices j of the flagged pieces, and
+//   slist[0 .. S) = the indices j of the first pieces of split segments, in
+//             no particular order (appended through atomic counters; the
+//             order in which they are processed does not affect any result)
 // Status word of a tile: flag << 62 | heads << 31 | pieces.
 __global__ void __launch_bounds__(kBlock) k_run_detect(
     const uint32_t* __restrict__ skey, const uint32_t* __restrict__ sperm, uint32_t n,
     uint4* __restrict__ rec, uint32_t* __restrict__ seg_off, uint32_t* __restrict__ mlist,
+    uint32_t* __restrict__ slist,
     unsigned long long* dstatus,
     uint32_t* tile_ctr, uint32_t* counts, int64_t* __restrict__ idx_out,
     int64_t* __restrict__ seg_off_out, int64_t* __restrict__ perm_out, int64_t* d_nnz_out,
     const int64_t* __restrict__ ls, int ls_per_coord, int64_t c, int64_t bound, int64_t t,
     int32_t* d_err)
 {
+    pdl_enter();
     constexpr unsigned long long kValMask = (1ull << 62) - 1ull;
     __shared__ uint32_t s_scan[kBlock / 32 + 1];
     __shared__ unsigned long long s_excl;
@@ -420,7 +435,7 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
 #pragma unroll
         for (int i = 0; i < kRunItems; ++i) pmv[i] = (p0 + i < n) ? sperm[p0 + i] : 0u;
     }
-    uint32_t nxt_key[kRunItems];
+    uint32_t nxt_key[kRunItems], long_key[kRunItems];
     int64_t last[kRunItems];
 #pragma unroll
     for (int i = 0; i < kRunItems; ++i) {
@@ -430,6 +445,7 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
         // multiple of kPieceLen that is >= q + kPieceLen
         const uint32_t nxt = (q + 2 * kPieceLen - 1) / kPieceLen * kPieceLen;
         nxt_key[i] = (h && nxt < n) ? skey[nxt] : ~k[i];
+        long_key[i] = (h && q + kShortLen < n) ? skey[q + kShortLen] : ~k[i];
         last[i] = (h && ls && !ls_per_coord && static_cast<int64_t>(k[i]) < bound) ? ls[k[i]] : 0;
     }
 #pragma unroll
@@ -459,10 +475,11 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
         const uint32_t pm = pmv[i];
         if (perm_out) perm_out[q] = static_cast<int64_t>(pm);
         if ((piecem >> i) & 1u) {
-            bool multi = true;
-            if (h) multi = (nxt_key[i] == k[i]);
-            rec[p_run] = make_uint4(q, k[i], u | (multi ? kMultiFlag : 0u), pm);
-            if (multi) mlist[atomicAdd(counts + kCntM, 1u)] = p_run;
+            uint32_t flag = kMultiFlag;
+            if (h) flag = (nxt_key[i] == k[i]) ? kMultiFlag : (long_key[i] == k[i] ? kLongFlag : 0u);
+            rec[p_run] = make_uint4(q, k[i], u | flag, pm);
+            if (flag) mlist[atomicAdd(counts + kCntM, 1u)] = p_run;
+            if (h && flag == kMultiFlag) slist[atomicAdd(counts + kCntS, 1u)] = p_run;
             ++p_run;
         }
     }
@@ -483,18 +500,12 @@ cudaError_t sort_and_segment(const int64_t* idx, int64_t n, int64_t c, int64_t b
                              int64_t* d_nnz_out, const int64_t* ls, int ls_per_coord, int64_t t,
                              int32_t* d_err, cudaStream_t s)
 {
-    cudaError_t e;
-    {
-        SO_PROFILE("memset_control", s);
-        e = cudaMemsetAsync(ws.gh, 0, L.ctrl_end - L.ctrl_begin, s);
-    }
-    if (e != cudaSuccess) return e;
     const uint32_t nn = static_cast<uint32_t>(n);
-    const int hist_blocks = static_cast<int>(
-        std::min<int64_t>((n + kBlock * kHistItems - 1) / (kBlock * kHistItems), 2 * num_sms()));
     {
         SO_PROFILE("range_hist", s);
-        k_range_hist<<<hist_blocks, kBlock, 0, s>>>(idx, nn, bound, L.passes, ws.gh, d_err);
+        launch(k_range_hist, dim3(L.hist_blocks), dim3(kBlock), s, idx, nn, bound, L.passes, ws.bh,
+               reinterpret_cast<uint4*>(ws.counts), static_cast<uint32_t>((L.ctrl_end - L.ctrl_begin) / 16),
+               d_err);
     }
     for (int p = 0; p < L.passes; ++p) {
         const int out = p & 1;
@@ -502,18 +513,18 @@ cudaError_t sort_and_segment(const int64_t* idx, int64_t n, int64_t c, int64_t b
         uint32_t* st = ws.rstatus + static_cast<size_t>(p) * L.sort_tiles * 256;
         SO_PROFILE("radix_pass", s);
         if (p == 0)
-            k_radix_pass<true><<<L.sort_tiles, kBlock, 0, s>>>(idx, nullptr, nullptr, ws.keys[out],
-                                                               ws.vals[out], nn, 8 * p, ws.gh + 256 * p, st,
+            launch(k_radix_pass<true>, dim3(L.sort_tiles), dim3(kBlock), s, idx, nullptr, nullptr, ws.keys[out],
+                                                               ws.vals[out], nn, 8 * p, ws.bh + 256 * p, L.hist_blocks, st,
                                                                ws.counts + kCtrPass0 + p, d_err);
         else
-            k_radix_pass<false><<<L.sort_tiles, kBlock, 0, s>>>(nullptr, ws.keys[in], ws.vals[in],
+            launch(k_radix_pass<false>, dim3(L.sort_tiles), dim3(kBlock), s, nullptr, ws.keys[in], ws.vals[in],
                                                                 ws.keys[out], ws.vals[out], nn, 8 * p,
-                                                                ws.gh + 256 * p, st,
+                                                                ws.bh + 256 * p, L.hist_blocks, st,
                                                                 ws.counts + kCtrPass0 + p, d_err);
     }
     SO_PROFILE("run_detect", s);
-    k_run_detect<<<L.run_tiles, kBlock, 0, s>>>(ws.keys[ws.final_buf], ws.vals[ws.final_buf], nn, ws.rec,
-                                                ws.seg_off, ws.mlist, ws.dstatus, ws.counts + kCtrRun, ws.counts,
+    launch(k_run_detect, dim3(L.run_tiles), dim3(kBlock), s, ws.keys[ws.final_buf], ws.vals[ws.final_buf], nn, ws.rec,
+                                                ws.seg_off, ws.mlist, ws.slist, ws.dstatus, ws.counts + kCtrRun, ws.counts,
                                                 idx_out, seg_off_out, perm_out, d_nnz_out, ls, ls_per_coord,
                                                 c, bound, t, d_err);
     return cudaGetLastError();
@@ -524,6 +535,7 @@ __global__ void __launch_bounds__(kBlock) k_check_rows(const int64_t* __restrict
                                                        int64_t r, int64_t c, const int64_t* __restrict__ ls,
                                                        int ls_per_coord, int64_t t, int32_t* d_err)
 {
+    pdl_enter();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; i < n; i += stride) {
         const int64_t k = rows[i];
@@ -552,7 +564,7 @@ cudaError_t check_canonical_rows(const int64_t* rows, int64_t n, int64_t r, int6
     const int blocks = static_cast<int>(std::max<int64_t>(
         1, std::min<int64_t>((n + kBlock - 1) / kBlock, 8 * num_sms())));
     SO_PROFILE("check_rows", s);
-    k_check_rows<<<blocks, kBlock, 0, s>>>(rows, n, r, c, ls, ls_per_coord, t, d_err);
+    launch(k_check_rows, dim3(blocks), dim3(kBlock), s, rows, n, r, c, ls, ls_per_coord, t, d_err);
     return cudaGetLastError();
 }
 
