@@ -51,6 +51,7 @@ constexpr int kSortTile = kBlock * kSortItems;
 constexpr int kRunItems = 8;           // sorted entries per thread in run detection
 constexpr int kRunTile = kBlock * kRunItems;
 constexpr int kMaxPasses = 4;          // 8-bit digits, keys < 2^32
+constexpr int kGroup = 32;             // pieces of a split segment merged by one team first
 constexpr int kHistItems = 8;          // keys a histogram thread requests at once
 #ifndef SO_HIST_BLOCKS
 #define SO_HIST_BLOCKS 32
@@ -162,14 +163,14 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* tmp, u
 struct WsLayout {
     int64_t n, c, nb;
     int passes, sort_tiles, run_tiles, hist_blocks;
-    size_t keys0, keys1, vals0, vals1, rec, seg_off, mlist, slist, part, bh;
+    size_t keys0, keys1, vals0, vals1, rec, seg_off, mlist, slist, glist, part, bh;
     size_t ctrl_begin, counts, rstatus, dstatus, ctrl_end;
     size_t total;
 };
 
 // counts[] word indices
-enum { kCtrHist = 0, kCtrPass0 = 1, kCtrRun = 5, kCntU = 8, kCntP = 9, kCntM = 10, kCntS = 11, kTicketM = 12,
-       kTicketS = 13, kCountsWords = 16 };
+enum { kCtrPass0 = 1, kCtrRun = 5, kCntU = 8, kCntP = 9, kCntM = 10, kCntS = 11, kCntG = 12, kTicketM = 13,
+       kTicketS = 14, kCountsWords = 16 };
 
 WsLayout ws_layout(int64_t n, int64_t c, int64_t bound);
 
@@ -181,9 +182,10 @@ struct SortWs {
     uint32_t* seg_off;    // [U+1]
     uint32_t* mlist;      // [M] indices of the long pieces (any order)
     uint32_t* slist;      // [S] indices of the first pieces of split segments (any order)
+    uint32_t* glist;      // [G] indices of the pieces heading a combine group (any order)
     float* part;          // partial sums: [2*nb slots][2][c]
     uint32_t* bh;         // [hist_blocks][4][256] digit histograms, one set per block
-    uint32_t* counts;     // [16]: tile counters, U, P, M, S, work tickets
+    uint32_t* counts;     // [16]: tile counters, U, P, M, S, G, work tickets
     uint32_t* rstatus;    // [passes][sort_tiles][256]
     unsigned long long* dstatus;  // [run_tiles]
     int final_buf;        // which keys/vals buffer holds the sorted result

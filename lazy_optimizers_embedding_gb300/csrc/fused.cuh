@@ -51,7 +51,6 @@ constexpr int kFusedMinBlocks = SO_FUSED_MIN_BLOCKS;
 constexpr int kTicket = SO_TICKET;
 constexpr int kRowIlp = SO_ROW_ILP;
 constexpr int kCombineBlock = 128;
-constexpr int kGroup = 32;   // pieces merged by one team in the first combine stage
 constexpr int kCombineIlp = SO_COMBINE_ILP;
 
 struct PieceInfo {
@@ -71,12 +70,15 @@ struct SortedSrc {
     const uint32_t* seg_off;
     const uint32_t* mlist;
     const uint32_t* slist;
+    const uint32_t* glist;
     const uint32_t* counts;
     __device__ __forceinline__ int64_t count() const { return counts[kCntP]; }
     __device__ __forceinline__ int64_t count_multi() const { return counts[kCntM]; }
     __device__ __forceinline__ int64_t multi_index(int64_t t) const { return mlist[t]; }
     __device__ __forceinline__ int64_t count_split() const { return counts[kCntS]; }
     __device__ __forceinline__ int64_t split_index(int64_t t) const { return slist[t]; }
+    __device__ __forceinline__ int64_t count_groups() const { return counts[kCntG]; }
+    __device__ __forceinline__ int64_t group_index(int64_t t) const { return glist[t]; }
     static constexpr bool kTickets = true;
     __device__ __forceinline__ uint32_t* ticket(int which) const { return const_cast<uint32_t*>(counts) + which; }
     __device__ __forceinline__ PieceInfo piece(int64_t j) const
@@ -109,6 +111,8 @@ struct CanonSrc {
     __device__ __forceinline__ int64_t multi_index(int64_t) const { return 0; }
     __device__ __forceinline__ int64_t count_split() const { return 0; }
     __device__ __forceinline__ int64_t split_index(int64_t) const { return 0; }
+    __device__ __forceinline__ int64_t count_groups() const { return 0; }
+    __device__ __forceinline__ int64_t group_index(int64_t) const { return 0; }
     static constexpr bool kTickets = false;
     __device__ __forceinline__ uint32_t* ticket(int) const { return nullptr; }
     __device__ __forceinline__ PieceInfo piece(int64_t j) const
@@ -163,7 +167,7 @@ __device__ __forceinline__ void ld_grad(const float* p, float (&x)[V])
     }
 }
 
-// partials are exchanged between blocks through L2
+// partials are exchanged between kernels through L2
 template <int V>
 __device__ __forceinline__ void ld_part(const float* p, float (&x)[V])
 {
@@ -176,14 +180,28 @@ __device__ __forceinline__ void ld_part(const float* p, float (&x)[V])
     }
 }
 
+// Partials are written long before the combine kernels read them, with the
+// whole step's gradient and state streaming through L2 in between: they are
+// stored with an L2 evict-last policy so that the combine reads hit L2.
+__device__ __forceinline__ uint64_t l2_keep_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 template <int V>
 __device__ __forceinline__ void st_part(float* p, const float (&x)[V])
 {
+    const uint64_t pol = l2_keep_policy();
     if constexpr (V == 4) {
-        __stcg(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
+        asm volatile("st.global.cg.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(x[0]),
+                     "f"(x[1]), "f"(x[2]), "f"(x[3]), "l"(pol)
+                     : "memory");
     } else {
 #pragma unroll
-        for (int i = 0; i < V; ++i) __stcg(p + i, x[i]);
+        for (int i = 0; i < V; ++i)
+            asm volatile("st.global.cg.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p + i), "f"(x[i]), "l"(pol) : "memory");
     }
 }
 
@@ -452,6 +470,11 @@ __device__ __forceinline__ int64_t part_slot(int64_t start, int64_t nb)
 {
     return (start % kPieceLen == 0) ? start / kPieceLen : nb + start / kPieceLen;
 }
+// Combine groups: piece i sits at the "aligned start" q1 + (i-1)*kPieceLen (its
+// true start for i >= 1, a multiple of kPieceLen), and a group is the pieces
+// whose aligned starts share a block of kGroup*kPieceLen positions (at most
+// kGroup pieces).  Its head, the piece run detection lists, is the segment's
+// first piece or the piece starting at the block boundary.
 struct SplitSegment {
     int64_t s0, s1, q1;
     __device__ __forceinline__ SplitSegment(int64_t a, int64_t b)
@@ -459,6 +482,13 @@ struct SplitSegment {
     __device__ __forceinline__ int64_t pieces() const { return (s1 - 1 >= q1) ? 2 + (s1 - 1 - q1) / kPieceLen : 1; }
     __device__ __forceinline__ int64_t start(int64_t i) const { return i == 0 ? s0 : q1 + (i - 1) * kPieceLen; }
     __device__ __forceinline__ int64_t index(int64_t st) const { return st == s0 ? 0 : (st - q1) / kPieceLen + 1; }
+    __device__ __forceinline__ int64_t group(int64_t i) const { return (q1 + (i - 1) * kPieceLen) / kGroupSpan; }
+    // index of the first piece of group g (the segment's first group: piece 0)
+    __device__ __forceinline__ int64_t group_head(int64_t g) const
+    {
+        return g == group(0) ? 0 : (g * kGroupSpan - q1) / kPieceLen + 1;
+    }
+    static constexpr int64_t kGroupSpan = static_cast<int64_t>(kGroup) * kPieceLen;
 };
 
 // Loads the optimizer state of one row chunk (the live arrays of the epilogue).
@@ -663,11 +693,11 @@ __global__ void __launch_bounds__(kBlock, kFusedMinBlocks) k_fused_rows(Src src,
     }
 }
 
-// Merges the partial pairs of pieces i0, i0 + step, ... (cnt of them) of a split
+// Merges the partial pairs of pieces piece_of(0), ..., piece_of(cnt-1) of a split
 // segment, in that order, at this lane's columns of the chunk at col0.
-template <int T, int NV, int V>
+template <int T, int NV, int V, class PieceOf>
 __device__ __forceinline__ void merge_partials(const float* __restrict__ part, int64_t c, int64_t nb,
-                                               const SplitSegment& seg, int64_t i0, int64_t step, int64_t cnt,
+                                               const SplitSegment& seg, PieceOf piece_of, int64_t cnt,
                                                int64_t col0, int tl, float (&S)[NV][V], float (&C)[NV][V])
 {
     constexpr int MR = NV >= kCombineIlp ? 1 : kCombineIlp / NV;   // partial pairs requested at once
@@ -676,7 +706,7 @@ __device__ __forceinline__ void merge_partials(const float* __restrict__ part, i
 #pragma unroll
         for (int r = 0; r < MR; ++r) {
             if (m0 + r < cnt) {
-                const float* ps = part + part_slot(seg.start(i0 + (m0 + r) * step), nb) * 2 * c;
+                const float* ps = part + part_slot(seg.start(piece_of(m0 + r)), nb) * 2 * c;
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
                     const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
@@ -706,9 +736,9 @@ __device__ __forceinline__ void merge_partials(const float* __restrict__ part, i
     }
 }
 
-// First combine stage: the pieces of every split segment in groups of kGroup
-// consecutive pieces (one team per group, found through its first piece, whose
-// slot receives the group's merged pair: the team has consumed that partial).
+// First combine stage: one team per combine group (listed by run detection
+// through its head piece) merges the group's partials in piece order into the
+// head's slot (the team has consumed that partial).
 template <int T, int NV, int V, class Src>
 __global__ void __launch_bounds__(kCombineBlock) k_combine_groups(Src src, int64_t c, float* __restrict__ part,
                                                                   int64_t nb, int32_t* d_err)
@@ -722,23 +752,22 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_groups(Src src, int64
     const int64_t team_g = static_cast<int64_t>(blockIdx.x) * kTeams + threadIdx.x / T;
     const int64_t nteams = static_cast<int64_t>(gridDim.x) * kTeams;
     const int nchunks = static_cast<int>((c + CW - 1) / CW);
-    const int64_t M = src.count_multi();
-    for (int64_t t = team_g; t < M; t += nteams) {
-        const PieceInfo pc = src.piece(src.multi_index(t));
-        if (!pc.multi()) continue;
+    const int64_t G = src.count_groups();
+    for (int64_t t = team_g; t < G; t += nteams) {
+        const PieceInfo pc = src.piece(src.group_index(t));
         int64_t s0, s1;
         src.seg_bounds(pc.u, s0, s1);
         const SplitSegment seg(s0, s1);
         const int64_t i = seg.index(pc.start);
-        if (i % kGroup != 0) continue;
         const int64_t K = seg.pieces();
-        const int64_t cnt = (K - i) < kGroup ? (K - i) : kGroup;
+        const int64_t next = seg.group_head(seg.group(i) + 1);
+        const int64_t cnt = (next < K ? next : K) - i;
         if (cnt < 2) continue;
         float* pd = part + part_slot(pc.start, nb) * 2 * c;
         for (int cc = 0; cc < nchunks; ++cc) {
             const int64_t col0 = static_cast<int64_t>(cc) * CW;
             float S[NV][V], C[NV][V];
-            merge_partials<T, NV, V>(part, c, nb, seg, i, 1, cnt, col0, tl, S, C);
+            merge_partials<T, NV, V>(part, c, nb, seg, [i](int64_t k) { return i + k; }, cnt, col0, tl, S, C);
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
                 const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
@@ -752,7 +781,8 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_groups(Src src, int64
 }
 
 // Second combine stage: one team per split segment merges its groups' pairs in
-// group order and applies the update.
+// group order (each group's pair sits in its head piece's slot) and applies the
+// update.
 template <int T, int NV, int V, class Src, class Epi>
 __global__ void __launch_bounds__(kCombineBlock) k_combine_final(Src src, int64_t c, Epi epi,
                                                                  const float* __restrict__ part, int64_t nb,
@@ -775,7 +805,8 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_final(Src src, int64_
         int64_t s0, s1;
         src.seg_bounds(pc.u, s0, s1);
         const SplitSegment seg(s0, s1);
-        const int64_t ng = (seg.pieces() + kGroup - 1) / kGroup;
+        const int64_t g0 = seg.group(0);
+        const int64_t ng = seg.group(seg.pieces() - 1) - g0 + 1;
         const int64_t* lp = epi.stage_last(pc);
         const int64_t last = lp ? *lp : 0;
         const typename Epi::Row row = epi.make_row(pc, last);
@@ -784,7 +815,8 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_final(Src src, int64_
             float x[NV][A][V];
             load_state<T, NV, V>(epi, pc, c, col0, tl, x);
             float S[NV][V], C[NV][V];
-            merge_partials<T, NV, V>(part, c, nb, seg, 0, kGroup, ng, col0, tl, S, C);
+            merge_partials<T, NV, V>(part, c, nb, seg, [&seg, g0](int64_t k) { return seg.group_head(g0 + k); },
+                                     ng, col0, tl, S, C);
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
                 const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
@@ -831,7 +863,8 @@ cudaError_t launch_shape(const Src& src, int64_t max_pieces, int64_t max_split, 
         const int64_t cap = static_cast<int64_t>(occ) * num_sms();
         {
             SO_PROFILE(Epi::kGroupsName, s);
-            const int64_t gb = std::min<int64_t>(cap, (2 * nb + kCTeams - 1) / kCTeams);
+            const int64_t groups = nb + nb / kGroup + 2;   // bound on the combine groups
+            const int64_t gb = std::min<int64_t>(cap, (groups + kCTeams - 1) / kCTeams);
             launch(k_combine_groups<T, NV, V, Src>, dim3(static_cast<unsigned>(gb)), dim3(kCombineBlock), s, src, c, part, nb,
                                                                                                d_err);
             const cudaError_t e = cudaGetLastError();
@@ -878,7 +911,7 @@ cudaError_t launch_fused(const Src& src, int64_t max_pieces, int64_t max_split, 
 
 inline SortedSrc sorted_src(const SortWs& ws)
 {
-    return SortedSrc{ws.rec, ws.vals[ws.final_buf], ws.seg_off, ws.mlist, ws.slist, ws.counts};
+    return SortedSrc{ws.rec, ws.vals[ws.final_buf], ws.seg_off, ws.mlist, ws.slist, ws.glist, ws.counts};
 }
 
 }  // namespace so

@@ -64,6 +64,7 @@ WsLayout ws_layout(int64_t n, int64_t c, int64_t bound)
     L.seg_off = take(sizeof(uint32_t) * (size_t)(n + 1));
     L.mlist = take(sizeof(uint32_t) * (size_t)(n + L.nb + 2));
     L.slist = take(sizeof(uint32_t) * (size_t)(L.nb + 1));
+    L.glist = take(sizeof(uint32_t) * (size_t)(L.nb + n / (kPieceLen * kGroup) + 2));
     L.part = take(sizeof(float) * (size_t)(2 * L.nb) * 2 * (size_t)c);
     L.hist_blocks = (int)std::min<int64_t>((n + kBlock * kHistItems - 1) / (kBlock * kHistItems), kMaxHistBlocks);
     L.bh = take(sizeof(uint32_t) * (size_t)L.hist_blocks * kMaxPasses * 256);
@@ -89,6 +90,7 @@ SortWs carve(const WsLayout& L, void* ws)
     w.seg_off = reinterpret_cast<uint32_t*>(b + L.seg_off);
     w.mlist = reinterpret_cast<uint32_t*>(b + L.mlist);
     w.slist = reinterpret_cast<uint32_t*>(b + L.slist);
+    w.glist = reinterpret_cast<uint32_t*>(b + L.glist);
     w.part = reinterpret_cast<float*>(b + L.part);
     w.bh = reinterpret_cast<uint32_t*>(b + L.bh);
     w.counts = reinterpret_cast<uint32_t*>(b + L.counts);
@@ -188,6 +190,12 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
     const uint32_t base = tile * kSortTile;
     const uint32_t tile_n = min(static_cast<uint32_t>(kSortTile), n - base);
 
+    // digit tid over the whole input: the histogram blocks' counts of this pass,
+    // requested together with the tile's keys
+    uint32_t hcount[kMaxHistBlocks];
+#pragma unroll
+    for (int q = 0; q < kMaxHistBlocks; ++q)
+        hcount[q] = (q < hist_blocks) ? bh[static_cast<size_t>(q) * kMaxPasses * 256 + tid] : 0u;
     uint32_t key[kSortItems], val[kSortItems], rank[kSortItems];
     int dig[kSortItems];
 #pragma unroll
@@ -237,15 +245,9 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
 
     uint32_t total;
     s_texcl[tid] = block_excl_scan(tcount, s_scan, &total);
-    uint32_t gcount = 0;   // digit tid over the whole input: the blocks' histograms of this pass
-    for (int b0 = 0; b0 < hist_blocks; b0 += 8) {
-        uint32_t h[8];
+    uint32_t gcount = 0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            h[q] = (b0 + q < hist_blocks) ? bh[static_cast<size_t>(b0 + q) * kMaxPasses * 256 + tid] : 0u;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) gcount += h[q];
-    }
+    for (int q = 0; q < kMaxHistBlocks; ++q) gcount += hcount[q];
     const uint32_t gexcl = block_excl_scan(gcount, s_scan, &total);
 
     // look-back: kLook predecessor words per round trip, consumed nearest first
@@ -322,14 +324,18 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
 //             | kLongFlag if it is one piece of more than kShortLen entries,
 //             input position of the start}, rec[P] = {n, 0, 0, 0}
 //   mlist[0 .. M) = the indices j of the flagged pieces, and
-//   slist[0 .. S) = the indices j of the first pieces of split segments, in
-//             no particular order (appended through atomic counters; the
-//             order in which they are processed does not affect any result)
+//   slist[0 .. S) = the indices j of the first pieces of split segments,
+//   glist[0 .. G) = the indices j of the pieces that head a combine group: the
+//             first piece of a split segment, and a later piece of one that
+//             starts at a multiple of kPieceLen*kGroup,
+//             each in no particular order (appended through atomic counters,
+//             one per list and warp; the order in which they are processed
+//             does not affect any result)
 // Status word of a tile: flag << 62 | heads << 31 | pieces.
 __global__ void __launch_bounds__(kBlock) k_run_detect(
     const uint32_t* __restrict__ skey, const uint32_t* __restrict__ sperm, uint32_t n,
     uint4* __restrict__ rec, uint32_t* __restrict__ seg_off, uint32_t* __restrict__ mlist,
-    uint32_t* __restrict__ slist,
+    uint32_t* __restrict__ slist, uint32_t* __restrict__ glist,
     unsigned long long* dstatus,
     uint32_t* tile_ctr, uint32_t* counts, int64_t* __restrict__ idx_out,
     int64_t* __restrict__ seg_off_out, int64_t* __restrict__ perm_out, int64_t* d_nnz_out,
@@ -448,6 +454,9 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
         long_key[i] = (h && q + kShortLen < n) ? skey[q + kShortLen] : ~k[i];
         last[i] = (h && ls && !ls_per_coord && static_cast<int64_t>(k[i]) < bound) ? ls[k[i]] : 0;
     }
+    uint32_t lists[kRunItems];   // flagged pieces of this thread, in order
+    uint32_t kinds = 0;          // 3 bits per flagged piece: long, split head, group head
+    int nl = 0;
 #pragma unroll
     for (int i = 0; i < kRunItems; ++i) {
         const uint32_t q = p0 + i;
@@ -478,10 +487,37 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
             uint32_t flag = kMultiFlag;
             if (h) flag = (nxt_key[i] == k[i]) ? kMultiFlag : (long_key[i] == k[i] ? kLongFlag : 0u);
             rec[p_run] = make_uint4(q, k[i], u | flag, pm);
-            if (flag) mlist[atomicAdd(counts + kCntM, 1u)] = p_run;
-            if (h && flag == kMultiFlag) slist[atomicAdd(counts + kCntS, 1u)] = p_run;
+            if (flag) {
+                lists[nl] = p_run;
+                kinds |= ((h && flag == kMultiFlag ? 2u : 0u) |
+                          (flag == kMultiFlag && (h || q % (kPieceLen * kGroup) == 0) ? 4u : 0u) | 1u)
+                         << (3 * nl);
+                ++nl;
+            }
             ++p_run;
         }
+    }
+    // the flagged pieces of the thread go to the long-piece, split-segment and
+    // combine-group lists: one atomic per list and warp
+    const int lane_w = tid & 31;
+#pragma unroll
+    for (int li = 0; li < 3; ++li) {
+        uint32_t mine = 0;
+        for (int e = 0; e < nl; ++e) mine += (kinds >> (3 * e + li)) & 1u;
+        uint32_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane_w >= o) incl += y;
+        }
+        const uint32_t wtotal = __shfl_sync(kFull, incl, 31);
+        uint32_t basew = 0;
+        if (lane_w == 31 && wtotal) basew = atomicAdd(counts + (li == 0 ? kCntM : li == 1 ? kCntS : kCntG), wtotal);
+        basew = __shfl_sync(kFull, basew, 31);
+        uint32_t* dst = li == 0 ? mlist : li == 1 ? slist : glist;
+        uint32_t at = basew + incl - mine;
+        for (int e = 0; e < nl; ++e)
+            if ((kinds >> (3 * e + li)) & 1u) dst[at++] = lists[e];
     }
     if (tile == gridDim.x - 1 && tid == 0) {
         const uint32_t U = static_cast<uint32_t>((ex + agg) >> 31);
@@ -524,7 +560,7 @@ cudaError_t sort_and_segment(const int64_t* idx, int64_t n, int64_t c, int64_t b
     }
     SO_PROFILE("run_detect", s);
     launch(k_run_detect, dim3(L.run_tiles), dim3(kBlock), s, ws.keys[ws.final_buf], ws.vals[ws.final_buf], nn, ws.rec,
-                                                ws.seg_off, ws.mlist, ws.slist, ws.dstatus, ws.counts + kCtrRun, ws.counts,
+                                                ws.seg_off, ws.mlist, ws.slist, ws.glist, ws.dstatus, ws.counts + kCtrRun, ws.counts,
                                                 idx_out, seg_off_out, perm_out, d_nnz_out, ls, ls_per_coord,
                                                 c, bound, t, d_err);
     return cudaGetLastError();
