@@ -404,6 +404,192 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------- other workloads
+# The other specified workloads, measured one GPU at a time with --workload (not the headline
+# line): a 1-D parameter with 1,000 unique ascending coordinates per step (Adam Lazy / DD, SGD),
+# a 1,000,000 x 64 table fed a CSR of summed Zipf(1.1) lookups, a 4,000,000 x 256 table fed an
+# element-granular CSR with per-coordinate state, and a 50,000,000 x 32 table fed raw uniform
+# lookups with lazy-momentum SGD.  Bytes per step as algorithmic traffic: state read + written
+# for every touched coordinate, last_step read (DormancyDecay) and written, gradient values,
+# indices / offsets / columns read.
+WORKLOADS = {
+    "d1_lazy": (wl.CFG_1D, "lazy"), "d1_dd": (wl.CFG_1D, "dd"), "d1_sgd": (wl.CFG_1D_SGD, None),
+    "zipf1m_csr": (wl.CFG_ZIPF_1M_64, "dd"), "csr4m": (wl.CFG_CSR_4M_256, "dd"),
+    "sgd50m": (wl.CFG_SGD_50M_32, None),
+}
+
+
+def run_workload(args):
+    import torch
+    from lazy_optimizers_embedding_gb300 import binding as so
+    import oracle
+    w, mode = WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    K, W = args.steps, args.warmup
+    nb = min(K + W, 8)
+    threads = os.cpu_count() or 8
+    c = w.cols
+    sgd = w.optimizer == "sgd"
+    dd = mode == "dd"
+    # host inputs: per batch the step's gradient, touched coordinates and algorithmic bytes
+    host, units, nbytes = [], [], []
+    for b in range(nb):
+        if w.index_dist == "csr_elem":
+            row_off, cols, vals = wl.csr_elem_step(w, b)
+            nnz = cols.shape[0]
+            host.append(("csr", row_off, cols, vals))
+            units.append(nnz)
+            nbytes.append(nnz * (24 + 16 if dd else 24 + 8) + nnz * 8 + (w.rows + 1) * 8)
+        elif args.workload == "zipf1m_csr":
+            idx, vals = wl.coo_step(w, b)
+            uidx, inv = np.unique(idx, return_inverse=True)
+            summed = np.zeros((uidx.shape[0], c), np.float64)
+            np.add.at(summed, inv, vals.astype(np.float64))
+            row_off = np.zeros(w.rows + 1, np.int64)
+            cnt = np.zeros(w.rows, np.int64)
+            cnt[uidx] = c
+            np.cumsum(cnt, out=row_off[1:])
+            cols = np.tile(np.arange(c, dtype=np.int32), uidx.shape[0])
+            host.append(("csr", row_off, cols, summed.astype(np.float32).reshape(-1)))
+            u = uidx.shape[0]
+            units.append(u * c)
+            nbytes.append(u * c * 24 + u * 16 + u * c * 8 + (w.rows + 1) * 8)
+        else:
+            idx, vals = wl.coo_step(w, b)
+            host.append(("coo", idx, vals))
+            u = int(np.unique(idx).shape[0])
+            units.append(u * c)
+            per = (16 if sgd else (24 + (16 if dd else 8)))   # state (+ last_step) bytes per coordinate
+            nbytes.append(u * c * per + idx.shape[0] * (8 + c * 4) if c > 1 else u * per + idx.shape[0] * 12)
+    p0 = wl.table_init(w, threads=threads)
+    p = torch.from_numpy(p0).to(dev).reshape(-1)
+    err = so.error_word(dev)
+    m = v = ls = buf = None
+    if sgd:
+        buf = torch.zeros_like(p)
+    else:
+        m, v = torch.zeros_like(p), torch.zeros_like(p)
+        ls = torch.zeros(p.numel() if (c == 1 or w.index_dist == "csr_elem") else w.rows, dtype=torch.int64,
+                         device=dev)
+    dev_in, grads, ws = [], [], None
+    for h in host:
+        if h[0] == "csr":
+            t3 = tuple(torch.from_numpy(a).to(dev) for a in h[1:])
+            dev_in.append(t3)
+            grads.append(so.csr(*t3))
+        else:
+            t2 = (torch.from_numpy(h[1]).to(dev), torch.from_numpy(h[2]).to(dev).reshape(h[1].shape[0], -1))
+            dev_in.append(t2)
+            grads.append(so.row_coo(t2[0], t2[1], w.index_dist == "unique_sorted"))
+    if any(h[0] == "coo" for h in host) and w.index_dist != "unique_sorted":
+        ws = so.workspace(w.lookups, c, w.rows, dev)
+    acfg = so.AdamConfig(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps)
+    scfg = so.SgdConfig(lr=w.lr, momentum=w.momentum, weight_decay=w.weight_decay)
+    amode = so.DORMANCY_DECAY if dd else so.LAZY
+    stream = torch.cuda.current_stream(dev)
+    state = {"t": 0}
+    per_coord = so.LAST_STEP_PER_COORD if (c == 1 or w.index_dist == "csr_elem") else so.LAST_STEP_PER_ROW
+
+    def step(b):
+        state["t"] += 1
+        if c == 1:
+            i, g = dev_in[b]
+            if sgd:
+                rc = so.sparse_sgd_step(p, buf, w.rows, i, g, i.numel(), 1, scfg, None, err, stream)
+            else:
+                rc = so.sparse_adam_step(p, m, v, ls, w.rows, i, g, i.numel(), 1, state["t"], acfg, amode, None,
+                                         err, stream)
+        elif sgd:
+            rc = so.sparse_sgd_table_step(p, buf, w.rows, c, grads[b], scfg, ws, err, stream)
+        else:
+            rc = so.sparse_adam_table_step(p, m, v, ls, per_coord, w.rows, c, grads[b], state["t"], acfg, amode,
+                                           ws, err, stream)
+        if rc:
+            raise RuntimeError(so.status_string(rc))
+
+    order = [i % nb for i in range(W + K)]
+    for i in range(W):
+        step(order[i])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(W, W + K):
+        step(order[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    el = e0.elapsed_time(e1) / 1e3
+    if int(err.item()):
+        raise RuntimeError(so.status_string(int(err.item())))
+    timed = order[W:]
+    u_tot = float(sum(units[b] for b in timed))
+    by_tot = float(sum(nbytes[b] for b in timed))
+    so.sparse_profile_reset()
+    so.sparse_profile_enable(True)
+    for b in timed:
+        step(b)
+    torch.cuda.synchronize()
+    prof = so.sparse_profile_read()
+    so.sparse_profile_enable(False)
+    dom, (dl, dms) = max(prof.items(), key=lambda kv: kv[1][1])
+    peak, peak_src = hbm_peak()
+    # the dominant kernel carries the step's state and gradient traffic (the CSR and row kernels)
+    dom_bytes = by_tot / K
+    dom_s = dms / 1e3 / max(1, dl)
+    # the oracle on the host: a bounded sample of the same steps
+    cpu = None
+    if not args.no_cpu_baseline:
+        hp = p0.reshape(-1).copy() if c == 1 else p0.copy()
+        hm = hv = hls = hbuf = None
+        if sgd:
+            hbuf = np.zeros_like(hp)
+        else:
+            hm, hv = np.zeros_like(hp), np.zeros_like(hp)
+            hls = np.zeros(hp.size if per_coord == so.LAST_STEP_PER_COORD else w.rows, np.int64)
+        spent, done, cu = 0.0, 0, 0
+        for k in range(K + W):
+            h = host[order[k]]
+            t0 = time.perf_counter()
+            if sgd and c == 1:
+                rc = oracle.sgd_step(hp, hbuf, h[1], h[2].reshape(-1), lr=w.lr, momentum=w.momentum,
+                                     weight_decay=w.weight_decay)
+            elif sgd:
+                rc = oracle.sgd_table_step(hp, hbuf, lr=w.lr, momentum=w.momentum, weight_decay=w.weight_decay,
+                                           rows=h[1], vals=h[2])
+            elif c == 1:
+                rc = oracle.adam_step(hp, hm, hv, hls, h[1], h[2].reshape(-1), k + 1, lr=w.lr, beta1=w.beta1,
+                                      beta2=w.beta2, eps=w.eps,
+                                      mode=oracle.MODE_DORMANCY_DECAY if dd else oracle.MODE_LAZY)
+            else:
+                kw = dict(row_off=h[1], cols=h[2], vals=h[3]) if h[0] == "csr" else dict(rows=h[1], vals=h[2])
+                rc = oracle.adam_table_step(hp, hm, hv, hls, k + 1, lr=w.lr, beta1=w.beta1, beta2=w.beta2,
+                                            eps=w.eps, mode=oracle.MODE_DORMANCY_DECAY if dd else oracle.MODE_LAZY,
+                                            ls_per_coord=per_coord == so.LAST_STEP_PER_COORD, **kw)
+            spent += time.perf_counter() - t0
+            assert rc == 0, rc
+            cu += units[order[k]]
+            done += 1
+            if spent >= args.cpu_seconds:
+                break
+        cpu = {"value": cu / spent, "unit": "coords/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {done} steps of the same workload; {spent:.1f} s of single-threaded oracle time"}
+    line = {"metric": METRIC, "value": u_tot / el, "unit": "coords/s", "n_gpus": 1, "steps": K, "warmup": W,
+            "ms_per_step": el / K * 1e3, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "mode": mode or "sgd", "rows": w.rows, "cols": c,
+                       "lookups_per_step": w.lookups, "distinct_batches": nb},
+            "achieved_hbm_gbs": by_tot / el / 1e9, "hbm_frac_of_peak": by_tot / el / 1e9 / peak,
+            "algorithmic_bytes_per_step": by_tot / K, "updated_coords_per_step": u_tot / K,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_bytes / dom_s / 1e9 if dom_s else None,
+                         "peak": peak, "unit": "GB/s",
+                         "frac": dom_bytes / dom_s / 1e9 / peak if dom_s else None, "traffic": None,
+                         "peak_source": peak_src, "avg_launch_us": dom_s * 1e6,
+                         "bytes_note": "the step's algorithmic bytes, all moved by this kernel"},
+            "kernel_share": {k: {"launches": l, "ms": ms} for k, (l, ms) in
+                             sorted(prof.items(), key=lambda kv: -kv[1][1])},
+            "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------------------- reference arm
 def run_reference(args):
     """The CPU oracle as the reference arm: same workload, metric and unit (rank 0 only)."""
@@ -445,6 +631,8 @@ def main(argv=None):
     ap.add_argument("--distinct", type=int, default=64, help="at most this many distinct input batches")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["zipf10m"] + sorted(WORKLOADS), default="zipf10m",
+                    help="another specified workload instead of the headline one (1 GPU, one JSON line)")
     ap.add_argument("--rows", type=int, default=None,
                     help="table rows (default 10,000,000); smaller tables are for ncu captures, not bench lines")
     args = ap.parse_args(argv)
@@ -452,7 +640,9 @@ def main(argv=None):
         globals()["W_CFG"] = W_CFG.scaled(name=f"{W_CFG.name}_rows{args.rows}", rows=args.rows)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.workload != "zipf10m":
+        run_workload(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
