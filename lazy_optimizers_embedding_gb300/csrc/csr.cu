@@ -17,6 +17,15 @@
 namespace so {
 
 constexpr int kMergeItems = 16;
+// Batches of full rows a warp requests at once in the check and in the update.
+#ifndef SO_CSR_CHECK_ILP
+#define SO_CSR_CHECK_ILP 4
+#endif
+#ifndef SO_CSR_ROW_ILP
+#define SO_CSR_ROW_ILP 2
+#endif
+constexpr int kCsrCheckIlp = SO_CSR_CHECK_ILP;
+constexpr int kCsrRowIlp = SO_CSR_ROW_ILP;
 
 struct Group {
     int64_t a, b;    // this lane's row: entries [a, b)
@@ -24,13 +33,34 @@ struct Group {
     bool ok;         // offsets of the group well formed
 };
 
+// The two offsets a lane needs for the group at r0 (requested ahead of use).
+struct GroupRaw {
+    int64_t a, last;
+};
+__device__ __forceinline__ GroupRaw fetch_group(const int64_t* __restrict__ row_off, int64_t r, int64_t r0, int lane)
+{
+    GroupRaw g{0, 0};
+    if (r0 < r) {
+        const int64_t rr = r0 + lane;
+        g.a = row_off[rr < r ? rr : r];
+        g.last = row_off[(r0 + 32) < r ? (r0 + 32) : r];
+    }
+    return g;
+}
+
+__device__ __forceinline__ Group make_group(const GroupRaw& raw, int64_t r, int64_t nnz, int64_t r0, int lane);
 __device__ __forceinline__ Group load_group(const int64_t* __restrict__ row_off, int64_t r, int64_t nnz,
                                             int64_t r0, int lane)
 {
+    return make_group(fetch_group(row_off, r, r0, lane), r, nnz, r0, lane);
+}
+
+__device__ __forceinline__ Group make_group(const GroupRaw& raw, int64_t r, int64_t nnz, int64_t r0, int lane)
+{
     Group G;
     const int64_t rr = r0 + lane;
-    G.a = row_off[rr < r ? rr : r];
-    const int64_t last = row_off[(r0 + 32) < r ? (r0 + 32) : r];
+    G.a = raw.a;
+    const int64_t last = raw.last;
     G.b = __shfl_down_sync(kFull, G.a, 1);
     if (lane == 31) G.b = last;
     G.lo = __shfl_sync(kFull, G.a, 0);
@@ -53,7 +83,27 @@ __device__ __forceinline__ int row_lane(const Group& G, int64_t j)
     return l;
 }
 
+// Full rows (all c columns listed, c = 4*TQ <= 128) are handled by sub-teams of
+// TQ lanes, one float4 of the row per lane, 32/TQ rows at a time and two such
+// batches requested together; the entries of the other rows are walked 32 at a
+// time, two chunks requested together, skipping the full rows.  fullmask has
+// bit l set when the group's row r0 + l is a full row taking that path.
+template <int TQ>
+__device__ __forceinline__ unsigned full_row_mask(const Group& G, int64_t r0, int64_t r, int64_t c)
+{
+    if constexpr (TQ == 0) {
+        return 0u;
+    } else {
+        const int64_t rr = r0 + (threadIdx.x & 31);
+        return __ballot_sync(kFull, rr < r && G.b - G.a == c && (G.a & 3) == 0);
+    }
+}
+
+// Lane l of the warp's k-th full row (k < popc(mask)).
+__device__ __forceinline__ int nth_row(unsigned mask, int k) { return static_cast<int>(__fns(mask, 0, k + 1)); }
+
 // Validation of a CSR gradient (and of last_step < t on its touched coordinates).
+template <int TQ>
 __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict__ row_off,
                                                       const int32_t* __restrict__ cols, int64_t r,
                                                       int64_t c, int64_t nnz, int full_rows,
@@ -66,10 +116,13 @@ __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict_
         set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
     const int64_t groups = (r + 31) / 32;
     const int64_t gstride = static_cast<int64_t>(gridDim.x) * (kBlock / 32);
-    for (int64_t gi = static_cast<int64_t>(blockIdx.x) * (kBlock / 32) + threadIdx.x / 32; gi < groups;
-         gi += gstride) {
+    int64_t gi = static_cast<int64_t>(blockIdx.x) * (kBlock / 32) + threadIdx.x / 32;
+    GroupRaw next = fetch_group(row_off, r, gi * 32, lane);
+    for (; gi < groups; gi += gstride) {
         const int64_t r0 = gi * 32;
-        const Group G = load_group(row_off, r, nnz, r0, lane);
+        const GroupRaw cur = next;
+        next = fetch_group(row_off, r, (gi + gstride) * 32, lane);   // the next group's offsets, in flight
+        const Group G = make_group(cur, r, nnz, r0, lane);
         if (!G.ok) {
             if (lane == 0) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
             continue;
@@ -79,87 +132,234 @@ __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict_
             if (full_rows && G.b - G.a != c) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
             if (ls && !ls_per_coord && ls[rr] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
         }
-        for (int64_t base = G.lo; base < G.hi; base += 32) {
-            const int64_t j = base + lane;
-            const int l = row_lane(G, j);
-            const int64_t start = __shfl_sync(kFull, G.a, l);
-            if (j >= G.hi) continue;
-            const int32_t col = cols[j];
-            if (col < 0 || col >= c) {
-                set_error(d_err, SPARSE_ERR_INDEX_OUT_OF_RANGE);
-                continue;
+        const unsigned fullmask = full_row_mask<TQ>(G, r0, r, c);
+        if constexpr (TQ > 0) {
+            // a listed full row is canonical iff its columns are exactly 0 .. c-1
+            constexpr int RPI = 32 / TQ;
+            const int sub = lane / TQ, q = lane % TQ;
+            const int nfull = __popc(fullmask);
+            constexpr int U = kCsrCheckIlp;   // batches of rows whose columns are requested together
+            for (int k0 = 0; k0 < nfull; k0 += U * RPI) {
+                int4 cc[U];
+                int lr[U];
+                bool act[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int k = k0 + u * RPI + sub;
+                    act[u] = k < nfull;
+                    lr[u] = act[u] ? nth_row(fullmask, k) : 0;
+                    const int64_t a = __shfl_sync(kFull, G.a, lr[u]);
+                    if (act[u]) cc[u] = *reinterpret_cast<const int4*>(cols + a + 4 * q);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (!act[u]) continue;
+                    const int want = 4 * q;
+                    if (cc[u].x != want || cc[u].y != want + 1 || cc[u].z != want + 2 || cc[u].w != want + 3) {
+                        const bool out = cc[u].x < 0 || cc[u].x >= c || cc[u].y < 0 || cc[u].y >= c ||
+                                         cc[u].z < 0 || cc[u].z >= c || cc[u].w < 0 || cc[u].w >= c;
+                        set_error(d_err, out ? SPARSE_ERR_INDEX_OUT_OF_RANGE : SPARSE_ERR_NOT_CANONICAL);
+                    }
+                    if (ls && ls_per_coord) {
+                        const int64_t i = (r0 + lr[u]) * c + 4 * q;
+                        for (int e = 0; e < 4; ++e)
+                            if (ls[i + e] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                    }
+                }
             }
-            if (j > start && cols[j - 1] >= col) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
-            if (ls && ls_per_coord && ls[(r0 + l) * c + col] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+        }
+        for (int64_t base = G.lo; base < G.hi; base += 64) {
+            int64_t j[2];
+            int l[2];
+            bool act[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                j[u] = base + 32 * u + lane;
+                l[u] = row_lane(G, j[u]);
+                act[u] = j[u] < G.hi && !((fullmask >> l[u]) & 1u);
+            }
+            if (!__any_sync(kFull, act[0] || act[1])) continue;
+            int32_t col[2], prev[2];
+            int64_t start[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                start[u] = __shfl_sync(kFull, G.a, l[u]);
+                col[u] = act[u] ? cols[j[u]] : 0;
+                prev[u] = (act[u] && j[u] > start[u]) ? cols[j[u] - 1] : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (!act[u]) continue;
+                if (col[u] < 0 || col[u] >= c) {
+                    set_error(d_err, SPARSE_ERR_INDEX_OUT_OF_RANGE);
+                    continue;
+                }
+                if (prev[u] >= col[u]) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
+                if (ls && ls_per_coord && ls[(r0 + l[u]) * c + col[u]] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+            }
         }
     }
 }
 
-// Element-granular update: every listed coordinate independently.  A per-row
-// last_step is read by every coordinate of the row and written once per row
-// after the whole group has read it.
-template <class Op>
+// Update.  Full rows go through the row epilogue of the fused kernels (128-bit
+// state and gradient loads); the other entries are updated one coordinate per
+// lane.  A per-row last_step is read by every coordinate of the row and written
+// once per row after the whole group has read it.
+template <class Op, class Epi, int TQ>
 __global__ void __launch_bounds__(kBlock) k_csr_update(const int64_t* __restrict__ row_off,
                                                        const int32_t* __restrict__ cols,
                                                        const float* __restrict__ vals, int64_t r, int64_t c,
-                                                       int64_t nnz, Op op, int32_t* d_err)
+                                                       int64_t nnz, Op op, Epi epi, int32_t* d_err)
 {
     pdl_enter();
     if (read_error(d_err)) return;
     const int lane = threadIdx.x & 31;
     const int64_t groups = (r + 31) / 32;
     const int64_t gstride = static_cast<int64_t>(gridDim.x) * (kBlock / 32);
-    for (int64_t gi = static_cast<int64_t>(blockIdx.x) * (kBlock / 32) + threadIdx.x / 32; gi < groups;
-         gi += gstride) {
+    int64_t gi = static_cast<int64_t>(blockIdx.x) * (kBlock / 32) + threadIdx.x / 32;
+    GroupRaw next = fetch_group(row_off, r, gi * 32, lane);
+    for (; gi < groups; gi += gstride) {
         const int64_t r0 = gi * 32;
-        const Group G = load_group(row_off, r, nnz, r0, lane);
+        const GroupRaw cur = next;
+        next = fetch_group(row_off, r, (gi + gstride) * 32, lane);   // the next group's offsets, in flight
+        const Group G = make_group(cur, r, nnz, r0, lane);
         if (!G.ok) continue;
-        for (int64_t base = G.lo; base < G.hi; base += 32) {
-            const int64_t j = base + lane;
-            const int l = row_lane(G, j);
-            if (j >= G.hi) continue;
-            op.coord(r0 + l, static_cast<int64_t>(__ldcs(cols + j)), __ldcs(vals + j));
+        const unsigned fullmask = full_row_mask<TQ>(G, r0, r, c);
+        if constexpr (TQ > 0) {
+            constexpr int RPI = 32 / TQ;
+            constexpr int A = Epi::kArrays;
+            const int sub = lane / TQ, q = lane % TQ;
+            const unsigned tmask = (TQ == 32) ? kFull : (((1u << TQ) - 1u) << (sub * TQ));
+            const int nfull = __popc(fullmask);
+            constexpr int U = kCsrRowIlp;   // batches of rows requested together
+            for (int k0 = 0; k0 < nfull; k0 += U * RPI) {
+                float x[U][A][4], g[U][4];
+                int64_t row[U], last[U];
+                bool act[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int k = k0 + u * RPI + sub;
+                    act[u] = k < nfull;
+                    const int l = act[u] ? nth_row(fullmask, k) : 0;
+                    const int64_t a = __shfl_sync(kFull, G.a, l);
+                    row[u] = r0 + l;
+                    last[u] = 0;
+                    if (act[u]) {
+                        const int64_t off = row[u] * c + 4 * q;
+#pragma unroll
+                        for (int ar = 0; ar < A; ++ar)
+                            if (ar < epi.arrays()) ld_state<4>(epi.array(ar) + off, x[u][ar]);
+                        ld_grad<4>(vals + a + 4 * q, g[u]);
+                        const int64_t* lp = op.row_last(row[u]);
+                        if (lp) last[u] = *lp;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (act[u]) {
+                        const typename Epi::Row rw = op.make_row(row[u], last[u]);
+                        epi.template apply<4>(rw, 4 * q, x[u], g[u]);
+                        epi.end_row(rw, q, tmask);
+                    }
+                }
+            }
+        }
+        for (int64_t base = G.lo; base < G.hi; base += 64) {
+            int64_t j[2];
+            int l[2];
+            bool act[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                j[u] = base + 32 * u + lane;
+                l[u] = row_lane(G, j[u]);
+                act[u] = j[u] < G.hi && !((fullmask >> l[u]) & 1u);
+            }
+            if (!__any_sync(kFull, act[0] || act[1])) continue;
+            int64_t col[2];
+            float g[2];
+            typename Op::Ld L[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                col[u] = act[u] ? static_cast<int64_t>(__ldcs(cols + j[u])) : 0;
+                g[u] = act[u] ? __ldcs(vals + j[u]) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (act[u]) L[u] = op.load(r0 + l[u], col[u]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (act[u]) op.store(r0 + l[u], col[u], L[u], g[u]);
         }
         __syncwarp();
         const int64_t rr = r0 + lane;
-        if (rr < r && G.b > G.a) op.row_done(rr);
+        if (rr < r && G.b > G.a && !((fullmask >> lane) & 1u)) op.row_done(rr);
     }
 }
 
 struct CsrAdamOp {
     AdamParams P;
     int64_t c;
-    __device__ __forceinline__ void coord(int64_t row, int64_t col, float g) const
+    struct Ld {
+        float p, m, v;
+        int64_t last;
+    };
+    __device__ __forceinline__ Ld load(int64_t row, int64_t col) const
+    {
+        const int64_t i = row * c + col;
+        Ld L;
+        L.p = P.p[i];
+        L.m = P.m[i];
+        L.v = P.v[i];
+        L.last = P.dd ? P.ls[P.ls_per_coord ? i : row] : 0;
+        return L;
+    }
+    __device__ __forceinline__ void store(int64_t row, int64_t col, Ld L, float g) const
     {
         const int64_t i = row * c + col;
         float b1 = P.beta1, b2 = P.beta2;
-        if (P.dd) dormancy_factors(P, P.t - P.ls[P.ls_per_coord ? i : row], b1, b2);
-        float p = P.p[i], m = P.m[i], v = P.v[i];
-        adam_coord(P, b1, b2, g, p, m, v);
-        P.p[i] = p;
-        P.m[i] = m;
-        P.v[i] = v;
+        if (P.dd) dormancy_factors(P, P.t - L.last, b1, b2);
+        adam_coord(P, b1, b2, g, L.p, L.m, L.v);
+        P.p[i] = L.p;
+        P.m[i] = L.m;
+        P.v[i] = L.v;
         if (P.ls_per_coord) P.ls[i] = P.t;
     }
     __device__ __forceinline__ void row_done(int64_t row) const
     {
         if (!P.ls_per_coord) P.ls[row] = P.t;
     }
+    // full-row path: the per-row last_step the epilogue needs (DormancyDecay, per-row layout)
+    __device__ __forceinline__ const int64_t* row_last(int64_t row) const
+    {
+        return (P.dd && !P.ls_per_coord) ? P.ls + row : nullptr;
+    }
+    __device__ __forceinline__ AdamEpi::Row make_row(int64_t row, int64_t last) const { return AdamEpi::Row{row, last}; }
 };
 
 struct CsrSgdOp {
     SgdParams P;
     int64_t c;
-    __device__ __forceinline__ void coord(int64_t row, int64_t col, float g) const
+    struct Ld {
+        float p, b;
+    };
+    __device__ __forceinline__ Ld load(int64_t row, int64_t col) const
     {
         const int64_t i = row * c + col;
-        float p = P.p[i];
-        float b = P.buf ? P.buf[i] : 0.0f;
-        sgd_coord(P, g, p, b);
-        P.p[i] = p;
-        if (P.buf) P.buf[i] = b;
+        Ld L;
+        L.p = P.p[i];
+        L.b = P.buf ? P.buf[i] : 0.0f;
+        return L;
+    }
+    __device__ __forceinline__ void store(int64_t row, int64_t col, Ld L, float g) const
+    {
+        const int64_t i = row * c + col;
+        sgd_coord(P, g, L.p, L.b);
+        P.p[i] = L.p;
+        if (P.buf) P.buf[i] = L.b;
     }
     __device__ __forceinline__ void row_done(int64_t) const {}
+    __device__ __forceinline__ const int64_t* row_last(int64_t) const { return nullptr; }
+    __device__ __forceinline__ SgdEpi::Row make_row(int64_t row, int64_t) const { return SgdEpi::Row{row}; }
 };
 
 static int group_blocks(int64_t r)
@@ -169,13 +369,39 @@ static int group_blocks(int64_t r)
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 16 * num_sms())));
 }
 
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Sub-team size for full rows of c columns (one float4 per lane), or 0 when the
+// rows take the per-coordinate path only.
+static int full_row_team(int64_t c, bool aligned)
+{
+    if (!aligned || c % 4 != 0 || c > 128) return 0;
+    const int64_t q = c / 4;
+    return (q & (q - 1)) == 0 ? static_cast<int>(q) : 0;
+}
+
+#define SO_TQ_DISPATCH(TQ, CALL)           \
+    switch (TQ) {                          \
+    case 1: CALL(1); break;                \
+    case 2: CALL(2); break;                \
+    case 4: CALL(4); break;                \
+    case 8: CALL(8); break;                \
+    case 16: CALL(16); break;              \
+    case 32: CALL(32); break;              \
+    default: CALL(0); break;               \
+    }
+
 cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, int64_t c, int64_t nnz,
                       int full_rows, const int64_t* ls, int ls_per_coord, int64_t t, int32_t* d_err,
                       cudaStream_t s)
 {
     SO_PROFILE("csr_check", s);
-    launch(k_csr_check, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, r, c, nnz, full_rows, ls, ls_per_coord, t,
-                                                   d_err);
+    const int tq = full_row_team(c, aligned16(cols));
+#define SO_CHECK(T)                                                                                              \
+    launch(k_csr_check<T>, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, r, c, nnz, full_rows, ls,        \
+           ls_per_coord, t, d_err)
+    SO_TQ_DISPATCH(tq, SO_CHECK)
+#undef SO_CHECK
     return cudaGetLastError();
 }
 
@@ -183,8 +409,13 @@ cudaError_t csr_adam(const int64_t* row_off, const int32_t* cols, const float* v
                      int64_t nnz, const AdamParams& P, int32_t* d_err, cudaStream_t s)
 {
     SO_PROFILE("csr_update_adam", s);
-    launch(k_csr_update<CsrAdamOp>, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, vals, r, c, nnz,
-                                                               CsrAdamOp{P, c}, d_err);
+    const int tq = full_row_team(c, aligned16(vals) && aligned16(P.p) && aligned16(P.m) && aligned16(P.v) &&
+                                        (!P.ls_per_coord || aligned16(P.ls)));
+#define SO_ADAM(T)                                                                                               \
+    launch(k_csr_update<CsrAdamOp, AdamEpi, T>, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, vals, r, c, \
+           nnz, CsrAdamOp{P, c}, AdamEpi{P, c}, d_err)
+    SO_TQ_DISPATCH(tq, SO_ADAM)
+#undef SO_ADAM
     return cudaGetLastError();
 }
 
@@ -192,8 +423,12 @@ cudaError_t csr_sgd(const int64_t* row_off, const int32_t* cols, const float* va
                     int64_t nnz, const SgdParams& P, int32_t* d_err, cudaStream_t s)
 {
     SO_PROFILE("csr_update_sgd", s);
-    launch(k_csr_update<CsrSgdOp>, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, vals, r, c, nnz,
-                                                              CsrSgdOp{P, c}, d_err);
+    const int tq = full_row_team(c, aligned16(vals) && aligned16(P.p) && (!P.buf || aligned16(P.buf)));
+#define SO_SGD(T)                                                                                                \
+    launch(k_csr_update<CsrSgdOp, SgdEpi, T>, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, vals, r, c,   \
+           nnz, CsrSgdOp{P, c}, SgdEpi{P, c}, d_err)
+    SO_TQ_DISPATCH(tq, SO_SGD)
+#undef SO_SGD
     return cudaGetLastError();
 }
 
