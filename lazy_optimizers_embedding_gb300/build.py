@@ -39,8 +39,17 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
+STAMP = os.path.join(BUILD, "defines.txt")   # the extra defines the current library was built with
+
+
 def _stale() -> bool:
     if not os.path.exists(LIB):
+        return True
+    try:
+        with open(STAMP) as f:
+            if f.read() != " ".join(EXTRA_DEFS):
+                return True
+    except OSError:
         return True
     t = os.path.getmtime(LIB)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
@@ -48,7 +57,7 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not _stale() and not EXTRA_DEFS:
+    if not force and not _stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
@@ -73,6 +82,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(" ".join(EXTRA_DEFS))
     return LIB
 
 

@@ -46,17 +46,32 @@ inline cudaError_t launch(void (*kernel)(P...), dim3 grid, dim3 block, cudaStrea
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kBlock = 256;            // threads per block of every kernel here
 constexpr int kPieceLen = 32;          // L: sorted entries summed by one team before a partial
-constexpr int kSortItems = 8;          // keys per thread in a radix pass
+#ifndef SO_SORT_ITEMS
+#define SO_SORT_ITEMS 8
+#endif
+#ifndef SO_RUN_ITEMS
+#define SO_RUN_ITEMS 8
+#endif
+constexpr int kSortItems = SO_SORT_ITEMS;   // keys per thread in a radix pass
 constexpr int kSortTile = kBlock * kSortItems;
-constexpr int kRunItems = 8;           // sorted entries per thread in run detection
+constexpr int kRunItems = SO_RUN_ITEMS;     // sorted entries per thread in run detection (a multiple of 4)
 constexpr int kRunTile = kBlock * kRunItems;
 constexpr int kMaxPasses = 4;          // 8-bit digits, keys < 2^32
 constexpr int kGroup = 32;             // pieces of a split segment merged by one team first
 constexpr int kHistItems = 8;          // keys a histogram thread requests at once
 #ifndef SO_HIST_BLOCKS
-#define SO_HIST_BLOCKS 32
+#define SO_HIST_BLOCKS 256
 #endif
-constexpr int kMaxHistBlocks = SO_HIST_BLOCKS;   // histogram blocks (each radix tile sums their counts)
+#ifndef SO_HIST_KEYS
+#define SO_HIST_KEYS 8192
+#endif
+#ifndef SO_RADIX_LOOK
+#define SO_RADIX_LOOK 4
+#endif
+constexpr int kMaxHistBlocks = SO_HIST_BLOCKS;     // histogram blocks at most
+constexpr int kHistKeysPerBlock = SO_HIST_KEYS;    // keys per histogram block (fewer blocks for small n)
+constexpr int kHistPrefetch = 32;                  // block counts a first-pass thread requests with its keys
+constexpr int kRadixLook = SO_RADIX_LOOK;          // predecessor tiles a radix look-back reads per round trip
 constexpr uint32_t kSingleMask = 0x3fffffffu;   // segment index bits of a piece record
 constexpr uint32_t kMultiFlag = 0x80000000u;    // piece of a segment split into several pieces
 constexpr uint32_t kLongFlag = 0x40000000u;     // whole segment of more than kShortLen entries
@@ -163,7 +178,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* tmp, u
 struct WsLayout {
     int64_t n, c, nb;
     int passes, sort_tiles, run_tiles, hist_blocks;
-    size_t keys0, keys1, vals0, vals1, rec, seg_off, mlist, slist, glist, part, bh;
+    size_t keys0, keys1, vals0, vals1, rec, seg_off, mlist, slist, glist, part, bh, gh;
     size_t ctrl_begin, counts, rstatus, dstatus, ctrl_end;
     size_t total;
 };
@@ -185,6 +200,7 @@ struct SortWs {
     uint32_t* glist;      // [G] indices of the pieces heading a combine group (any order)
     float* part;          // partial sums: [2*nb slots][2][c]
     uint32_t* bh;         // [hist_blocks][4][256] digit histograms, one set per block
+    uint32_t* gh;         // [4][256] whole-input digit histograms of the later passes
     uint32_t* counts;     // [16]: tile counters, U, P, M, S, G, work tickets
     uint32_t* rstatus;    // [passes][sort_tiles][256]
     unsigned long long* dstatus;  // [run_tiles]

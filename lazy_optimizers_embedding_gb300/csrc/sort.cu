@@ -66,8 +66,9 @@ WsLayout ws_layout(int64_t n, int64_t c, int64_t bound)
     L.slist = take(sizeof(uint32_t) * (size_t)(L.nb + 1));
     L.glist = take(sizeof(uint32_t) * (size_t)(L.nb + n / (kPieceLen * kGroup) + 2));
     L.part = take(sizeof(float) * (size_t)(2 * L.nb) * 2 * (size_t)c);
-    L.hist_blocks = (int)std::min<int64_t>((n + kBlock * kHistItems - 1) / (kBlock * kHistItems), kMaxHistBlocks);
+    L.hist_blocks = (int)std::min<int64_t>((n + kHistKeysPerBlock - 1) / kHistKeysPerBlock, kMaxHistBlocks);
     L.bh = take(sizeof(uint32_t) * (size_t)L.hist_blocks * kMaxPasses * 256);
+    L.gh = take(sizeof(uint32_t) * kMaxPasses * 256);
     off = align_up(off, 256);
     L.ctrl_begin = off;
     L.counts = take(sizeof(uint32_t) * kCountsWords);
@@ -93,6 +94,7 @@ SortWs carve(const WsLayout& L, void* ws)
     w.glist = reinterpret_cast<uint32_t*>(b + L.glist);
     w.part = reinterpret_cast<float*>(b + L.part);
     w.bh = reinterpret_cast<uint32_t*>(b + L.bh);
+    w.gh = reinterpret_cast<uint32_t*>(b + L.gh);
     w.counts = reinterpret_cast<uint32_t*>(b + L.counts);
     w.rstatus = reinterpret_cast<uint32_t*>(b + L.rstatus);
     w.dstatus = reinterpret_cast<unsigned long long*>(b + L.dstatus);
@@ -149,6 +151,21 @@ __global__ void __launch_bounds__(kBlock) k_range_hist(const int64_t* __restrict
     for (int i = threadIdx.x; i < passes * 256; i += kBlock) mine[i] = sh[i];
 }
 
+// Sum over histogram blocks b0 .. hb-1 of one digit's count (32 loads in flight).
+__device__ __forceinline__ uint32_t sum_hist(const uint32_t* __restrict__ bh, int b0, int hb, int digit)
+{
+    uint32_t s = 0;
+    for (int b = b0; b < hb; b += 32) {
+        uint32_t h[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+            h[q] = (b + q < hb) ? bh[static_cast<size_t>(b + q) * kMaxPasses * 256 + digit] : 0u;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) s += h[q];
+    }
+    return s;
+}
+
 // ---------------------------------------------------------------------- K2
 // One stable counting pass over digit (key >> shift) & 255.  Tiles are taken in
 // launch order from an atomic counter, so a tile only ever waits on tiles that
@@ -167,6 +184,7 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
                                                        uint32_t* __restrict__ kout,
                                                        uint32_t* __restrict__ vout, uint32_t n, int shift,
                                                        const uint32_t* __restrict__ bh, int hist_blocks,
+                                                       uint32_t* __restrict__ gh, int passes,
                                                        uint32_t* status, uint32_t* tile_ctr,
                                                        int32_t* d_err)
 {
@@ -190,12 +208,18 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
     const uint32_t base = tile * kSortTile;
     const uint32_t tile_n = min(static_cast<uint32_t>(kSortTile), n - base);
 
-    // digit tid over the whole input: the histogram blocks' counts of this pass,
-    // requested together with the tile's keys
-    uint32_t hcount[kMaxHistBlocks];
+    // digit tid over the whole input.  The first pass sums the histogram blocks'
+    // counts (the first kHistPrefetch requested together with the tile's keys)
+    // and tile t also writes the global histograms of passes 1 + t, 1 + t + tiles,
+    // ... for the later passes, which read them with one load.
+    uint32_t hcount[kHistPrefetch];
+    if (kFirst) {
 #pragma unroll
-    for (int q = 0; q < kMaxHistBlocks; ++q)
-        hcount[q] = (q < hist_blocks) ? bh[static_cast<size_t>(q) * kMaxPasses * 256 + tid] : 0u;
+        for (int q = 0; q < kHistPrefetch; ++q)
+            hcount[q] = (q < hist_blocks) ? bh[static_cast<size_t>(q) * kMaxPasses * 256 + tid] : 0u;
+    } else {
+        hcount[0] = gh[tid];
+    }
     uint32_t key[kSortItems], val[kSortItems], rank[kSortItems];
     int dig[kSortItems];
 #pragma unroll
@@ -246,14 +270,21 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
     uint32_t total;
     s_texcl[tid] = block_excl_scan(tcount, s_scan, &total);
     uint32_t gcount = 0;
+    if (kFirst) {
 #pragma unroll
-    for (int q = 0; q < kMaxHistBlocks; ++q) gcount += hcount[q];
+        for (int q = 0; q < kHistPrefetch; ++q) gcount += hcount[q];
+        gcount += sum_hist(bh, kHistPrefetch, hist_blocks, tid);
+        for (int p = 1 + static_cast<int>(tile); p < passes; p += static_cast<int>(gridDim.x))
+            gh[p * 256 + tid] = sum_hist(bh + p * 256, 0, hist_blocks, tid);
+    } else {
+        gcount = hcount[0];
+    }
     const uint32_t gexcl = block_excl_scan(gcount, s_scan, &total);
 
     // look-back: kLook predecessor words per round trip, consumed nearest first
     // until an inclusive one; a word not yet published stops the round (its
     // tile started earlier, so it publishes soon) and is read again.
-    constexpr int kLook = 4;
+    constexpr int kLook = kRadixLook;
     uint32_t excl = 0;
     if (tile > 0) {
         int64_t j = static_cast<int64_t>(tile) - 1;
@@ -358,10 +389,11 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     uint32_t prev = 0;
     if (p0 < n && p0 > 0) prev = skey[p0 - 1];
     if (p0 + kRunItems <= n) {
-        const uint4 a = *reinterpret_cast<const uint4*>(skey + p0);
-        const uint4 b = *reinterpret_cast<const uint4*>(skey + p0 + 4);
-        k[0] = a.x; k[1] = a.y; k[2] = a.z; k[3] = a.w;
-        k[4] = b.x; k[5] = b.y; k[6] = b.z; k[7] = b.w;
+#pragma unroll
+        for (int v4 = 0; v4 < kRunItems / 4; ++v4) {
+            const uint4 a = *reinterpret_cast<const uint4*>(skey + p0 + 4 * v4);
+            k[4 * v4] = a.x; k[4 * v4 + 1] = a.y; k[4 * v4 + 2] = a.z; k[4 * v4 + 3] = a.w;
+        }
     } else {
 #pragma unroll
         for (int i = 0; i < kRunItems; ++i) k[i] = (p0 + i < n) ? skey[p0 + i] : 0u;
@@ -433,10 +465,11 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     // the key at the next piece boundary of each segment head, last_step
     uint32_t pmv[kRunItems];
     if (p0 + kRunItems <= n) {
-        const uint4 a = *reinterpret_cast<const uint4*>(sperm + p0);
-        const uint4 b = *reinterpret_cast<const uint4*>(sperm + p0 + 4);
-        pmv[0] = a.x; pmv[1] = a.y; pmv[2] = a.z; pmv[3] = a.w;
-        pmv[4] = b.x; pmv[5] = b.y; pmv[6] = b.z; pmv[7] = b.w;
+#pragma unroll
+        for (int v4 = 0; v4 < kRunItems / 4; ++v4) {
+            const uint4 a = *reinterpret_cast<const uint4*>(sperm + p0 + 4 * v4);
+            pmv[4 * v4] = a.x; pmv[4 * v4 + 1] = a.y; pmv[4 * v4 + 2] = a.z; pmv[4 * v4 + 3] = a.w;
+        }
     } else {
 #pragma unroll
         for (int i = 0; i < kRunItems; ++i) pmv[i] = (p0 + i < n) ? sperm[p0 + i] : 0u;
@@ -455,7 +488,8 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
         last[i] = (h && ls && !ls_per_coord && static_cast<int64_t>(k[i]) < bound) ? ls[k[i]] : 0;
     }
     uint32_t lists[kRunItems];   // flagged pieces of this thread, in order
-    uint32_t kinds = 0;          // 3 bits per flagged piece: long, split head, group head
+    uint64_t kinds = 0;          // 3 bits per flagged piece: long, split head, group head
+    static_assert(3 * kRunItems <= 64, "kinds holds 3 bits per item");
     int nl = 0;
 #pragma unroll
     for (int i = 0; i < kRunItems; ++i) {
@@ -489,8 +523,9 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
             rec[p_run] = make_uint4(q, k[i], u | flag, pm);
             if (flag) {
                 lists[nl] = p_run;
-                kinds |= ((h && flag == kMultiFlag ? 2u : 0u) |
-                          (flag == kMultiFlag && (h || q % (kPieceLen * kGroup) == 0) ? 4u : 0u) | 1u)
+                kinds |= static_cast<uint64_t>((h && flag == kMultiFlag ? 2u : 0u) |
+                                               (flag == kMultiFlag && (h || q % (kPieceLen * kGroup) == 0) ? 4u : 0u) |
+                                               1u)
                          << (3 * nl);
                 ++nl;
             }
@@ -503,7 +538,7 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
 #pragma unroll
     for (int li = 0; li < 3; ++li) {
         uint32_t mine = 0;
-        for (int e = 0; e < nl; ++e) mine += (kinds >> (3 * e + li)) & 1u;
+        for (int e = 0; e < nl; ++e) mine += static_cast<uint32_t>((kinds >> (3 * e + li)) & 1u);
         uint32_t incl = mine;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -550,12 +585,12 @@ cudaError_t sort_and_segment(const int64_t* idx, int64_t n, int64_t c, int64_t b
         SO_PROFILE("radix_pass", s);
         if (p == 0)
             launch(k_radix_pass<true>, dim3(L.sort_tiles), dim3(kBlock), s, idx, nullptr, nullptr, ws.keys[out],
-                                                               ws.vals[out], nn, 8 * p, ws.bh + 256 * p, L.hist_blocks, st,
+                                                               ws.vals[out], nn, 8 * p, ws.bh, L.hist_blocks, ws.gh, L.passes, st,
                                                                ws.counts + kCtrPass0 + p, d_err);
         else
             launch(k_radix_pass<false>, dim3(L.sort_tiles), dim3(kBlock), s, nullptr, ws.keys[in], ws.vals[in],
                                                                 ws.keys[out], ws.vals[out], nn, 8 * p,
-                                                                ws.bh + 256 * p, L.hist_blocks, st,
+                                                                ws.bh, L.hist_blocks, ws.gh + 256 * p, L.passes, st,
                                                                 ws.counts + kCtrPass0 + p, d_err);
     }
     SO_PROFILE("run_detect", s);
