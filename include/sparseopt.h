@@ -51,6 +51,7 @@
  *             coordinate is touched when it is present in the canonical sparse
  *             structure, whatever its value; nothing else is read or written.
  *   Limits.   Raw (non-canonical) input: n <= 2^30 entries, keys < 2^32.
+ *             Canonical row-COO input: n < 2^31 rows.
  */
 #ifndef SPARSEOPT_H
 #define SPARSEOPT_H

@@ -44,23 +44,29 @@ namespace so {
 #ifndef SO_ROW_ILP
 #define SO_ROW_ILP 4
 #endif
+#ifndef SO_LONG_ILP
+#define SO_LONG_ILP 4
+#endif
 #ifndef SO_COMBINE_ILP
 #define SO_COMBINE_ILP 8
 #endif
 constexpr int kFusedMinBlocks = SO_FUSED_MIN_BLOCKS;
 constexpr int kTicket = SO_TICKET;
 constexpr int kRowIlp = SO_ROW_ILP;
+constexpr int kLongIlp = SO_LONG_ILP;   // gradient rows requested at once in a long piece
 constexpr int kCombineBlock = 128;
 constexpr int kCombineIlp = SO_COMBINE_ILP;
 
 struct PieceInfo {
-    int64_t start, end;   // sorted positions [start, end)
+    uint32_t start, end;  // sorted positions [start, end)
     int64_t key;          // table row
-    uint32_t u;           // segment index (row of a canonical output)
-    uint32_t flags;       // kMultiFlag: segment spans several pieces; kLongFlag: one long piece
+    uint32_t uf;          // segment index (row of a canonical output) | flags
     uint32_t perm0;       // input position of the first entry
-    __device__ __forceinline__ bool multi() const { return (flags & kMultiFlag) != 0u; }
-    __device__ __forceinline__ bool is_short() const { return flags == 0u; }
+    // kMultiFlag: segment spans several pieces; kLongFlag: one long piece
+    __device__ __forceinline__ uint32_t u() const { return uf & kSingleMask; }
+    __device__ __forceinline__ uint32_t flags() const { return uf & (kMultiFlag | kLongFlag); }
+    __device__ __forceinline__ bool multi() const { return (uf & kMultiFlag) != 0u; }
+    __device__ __forceinline__ bool is_short() const { return (uf & (kMultiFlag | kLongFlag)) == 0u; }
 };
 
 // Pieces of a raw input, from the sort and run detection.
@@ -89,8 +95,7 @@ struct SortedSrc {
         p.start = r.x;
         p.end = e;
         p.key = r.y;
-        p.u = r.z & kSingleMask;
-        p.flags = r.z & (kMultiFlag | kLongFlag);
+        p.uf = r.z;
         p.perm0 = r.w;
         return p;
     }
@@ -118,11 +123,10 @@ struct CanonSrc {
     __device__ __forceinline__ PieceInfo piece(int64_t j) const
     {
         PieceInfo p;
-        p.start = j;
-        p.end = j + 1;
+        p.start = static_cast<uint32_t>(j);
+        p.end = static_cast<uint32_t>(j + 1);
         p.key = rows[j];
-        p.u = static_cast<uint32_t>(j);
-        p.flags = 0u;
+        p.uf = static_cast<uint32_t>(j) & kSingleMask;
         p.perm0 = static_cast<uint32_t>(j);
         return p;
     }
@@ -352,7 +356,7 @@ struct StoreEpi {
         int64_t u;
     };
     __device__ __forceinline__ const int64_t* stage_last(const PieceInfo&) const { return nullptr; }
-    __device__ __forceinline__ Row make_row(const PieceInfo& pc, int64_t) const { return Row{pc.u}; }
+    __device__ __forceinline__ Row make_row(const PieceInfo& pc, int64_t) const { return Row{pc.u()}; }
     __device__ __forceinline__ int arrays() const { return 0; }
     __device__ __forceinline__ float* array(int) const { return nullptr; }
     __device__ __forceinline__ int64_t base(const PieceInfo&) const { return 0; }
@@ -566,11 +570,10 @@ template <int T>
 __device__ __forceinline__ PieceInfo shfl_piece(const PieceInfo& p, int from, unsigned tmask)
 {
     PieceInfo q;
-    q.start = __shfl_sync(tmask, static_cast<long long>(p.start), from, T);
-    q.end = __shfl_sync(tmask, static_cast<long long>(p.end), from, T);
+    q.start = __shfl_sync(tmask, p.start, from, T);
+    q.end = __shfl_sync(tmask, p.end, from, T);
     q.key = __shfl_sync(tmask, static_cast<long long>(p.key), from, T);
-    q.u = __shfl_sync(tmask, p.u, from, T);
-    q.flags = __shfl_sync(tmask, p.flags, from, T);
+    q.uf = __shfl_sync(tmask, p.uf, from, T);
     q.perm0 = __shfl_sync(tmask, p.perm0, from, T);
     return q;
 }
@@ -592,7 +595,7 @@ __device__ __forceinline__ void store_partial(const Src& src, const float* __res
         float s[NV][V], cm[NV][V];
         first_row<T, NV, V>(vals, c, col0, tl, pc.perm0, s);
         zero_comp<NV, V>(cm);
-        sum_rest<T, NV, V, kRowIlp>(src, pp, vals, c, col0, tl, tmask, pc, s, cm);
+        sum_rest<T, NV, V, kLongIlp>(src, pp, vals, c, col0, tl, tmask, pc, s, cm);
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
@@ -648,7 +651,7 @@ __global__ void __launch_bounds__(kBlock, kFusedMinBlocks) k_fused_rows(Src src,
                 if (pc.multi())
                     store_partial<T, NV, V>(src, vals, c, part, nb, pc, tl, tmask);
                 else
-                    apply_single<T, NV, V, kRowIlp>(src, vals, c, epi, pc, tl, tmask);
+                    apply_single<T, NV, V, kLongIlp>(src, vals, c, epi, pc, tl, tmask);
                 ta = tb;
                 ra = rb;
                 tb = __shfl_sync(tmask, tc, 0, T);
@@ -756,7 +759,7 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_groups(Src src, int64
     for (int64_t t = team_g; t < G; t += nteams) {
         const PieceInfo pc = src.piece(src.group_index(t));
         int64_t s0, s1;
-        src.seg_bounds(pc.u, s0, s1);
+        src.seg_bounds(pc.u(), s0, s1);
         const SplitSegment seg(s0, s1);
         const int64_t i = seg.index(pc.start);
         const int64_t K = seg.pieces();
@@ -803,7 +806,7 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_final(Src src, int64_
     for (int64_t t = team_g; t < S_; t += nteams) {
         const PieceInfo pc = src.piece(src.split_index(t));   // the segment's first piece
         int64_t s0, s1;
-        src.seg_bounds(pc.u, s0, s1);
+        src.seg_bounds(pc.u(), s0, s1);
         const SplitSegment seg(s0, s1);
         const int64_t g0 = seg.group(0);
         const int64_t ng = seg.group(seg.pieces() - 1) - g0 + 1;
