@@ -179,7 +179,7 @@ struct WsLayout {
     int64_t n, c, nb;
     int passes, sort_tiles, run_tiles, hist_blocks;
     size_t keys0, keys1, vals0, vals1, rec, seg_off, mlist, slist, glist, part, bh, gh;
-    size_t ctrl_begin, counts, rstatus, dstatus, ctrl_end;
+    size_t ctrl_begin, counts, rstatus, dstatus, scnt, ctrl_end;
     size_t total;
 };
 
@@ -204,6 +204,7 @@ struct SortWs {
     uint32_t* counts;     // [16]: tile counters, U, P, M, S, G, work tickets
     uint32_t* rstatus;    // [passes][sort_tiles][256]
     unsigned long long* dstatus;  // [run_tiles]
+    uint32_t* scnt;       // [2*nb] groups merged per split segment (zeroed with the control block)
     int final_buf;        // which keys/vals buffer holds the sorted result
 };
 

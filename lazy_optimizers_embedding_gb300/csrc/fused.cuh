@@ -11,11 +11,12 @@
 // applied directly: the team loads the row's optimizer state and the piece's
 // gradient rows together, sums the gradient with error-free TwoSum
 // compensation, updates and stores.  A segment that spans several pieces (a
-// heavy Zipf head) is reduced in two launches: the row kernel writes every
+// heavy Zipf head) is reduced in a second launch: the row kernel writes every
 // piece's compensated partial (sum, error) to a slot, then the combine kernel
-// merges each such segment's partials in piece order, one block per segment,
-// and applies the update.  The order of every addition is fixed, so results
-// are bit-reproducible, and no thread ever waits on another.
+// merges groups of kGroup consecutive pieces (one team each) and the last group
+// of each segment to finish merges the groups and applies the update.  The
+// order of every addition is fixed, so results are bit-reproducible, and no
+// thread ever waits on another.
 //
 // Sum of duplicates per "DiskSparseAdam (DSA)" README, "Safe Duplicate
 // Aggregation"; update rules per "Module sparse_optimizer" (optirs-gpu 0.3.2
@@ -78,6 +79,7 @@ struct SortedSrc {
     const uint32_t* slist;
     const uint32_t* glist;
     const uint32_t* counts;
+    uint32_t* scnt;   // groups of a split segment merged so far (by its first piece's slot)
     __device__ __forceinline__ int64_t count() const { return counts[kCntP]; }
     __device__ __forceinline__ int64_t count_multi() const { return counts[kCntM]; }
     __device__ __forceinline__ int64_t multi_index(int64_t t) const { return mlist[t]; }
@@ -85,6 +87,7 @@ struct SortedSrc {
     __device__ __forceinline__ int64_t split_index(int64_t t) const { return slist[t]; }
     __device__ __forceinline__ int64_t count_groups() const { return counts[kCntG]; }
     __device__ __forceinline__ int64_t group_index(int64_t t) const { return glist[t]; }
+    __device__ __forceinline__ uint32_t* segment_counter(int64_t slot) const { return scnt + slot; }
     static constexpr bool kTickets = true;
     __device__ __forceinline__ uint32_t* ticket(int which) const { return const_cast<uint32_t*>(counts) + which; }
     __device__ __forceinline__ PieceInfo piece(int64_t j) const
@@ -118,6 +121,7 @@ struct CanonSrc {
     __device__ __forceinline__ int64_t split_index(int64_t) const { return 0; }
     __device__ __forceinline__ int64_t count_groups() const { return 0; }
     __device__ __forceinline__ int64_t group_index(int64_t) const { return 0; }
+    __device__ __forceinline__ uint32_t* segment_counter(int64_t) const { return nullptr; }
     static constexpr bool kTickets = false;
     __device__ __forceinline__ uint32_t* ticket(int) const { return nullptr; }
     __device__ __forceinline__ PieceInfo piece(int64_t j) const
@@ -270,8 +274,7 @@ __device__ __forceinline__ void sgd_coord(const SgdParams& P, float g, float& p,
 // read before the update (stage_last) and rewritten after it (end_row).
 struct AdamEpi {
     static constexpr const char* kName = "fused_rows_adam";
-    static constexpr const char* kCombineName = "combine_final_adam";
-    static constexpr const char* kGroupsName = "combine_groups_adam";
+    static constexpr const char* kCombineName = "combine_split_adam";
     static constexpr int kArrays = 3;   // p, m, v
     AdamParams P;
     int64_t c;
@@ -319,8 +322,7 @@ struct AdamEpi {
 
 struct SgdEpi {
     static constexpr const char* kName = "fused_rows_sgd";
-    static constexpr const char* kCombineName = "combine_final_sgd";
-    static constexpr const char* kGroupsName = "combine_groups_sgd";
+    static constexpr const char* kCombineName = "combine_split_sgd";
     static constexpr int kArrays = 2;   // p, momentum buffer (absent without momentum)
     SgdParams P;
     int64_t c;
@@ -347,8 +349,7 @@ struct SgdEpi {
 // canonicalisation: write the summed row u
 struct StoreEpi {
     static constexpr const char* kName = "fused_rows_sum";
-    static constexpr const char* kCombineName = "combine_final_sum";
-    static constexpr const char* kGroupsName = "combine_groups_sum";
+    static constexpr const char* kCombineName = "combine_split_sum";
     static constexpr int kArrays = 1;   // no state; one dummy array keeps the types simple
     StoreParams P;
     int64_t c;
@@ -739,56 +740,16 @@ __device__ __forceinline__ void merge_partials(const float* __restrict__ part, i
     }
 }
 
-// First combine stage: one team per combine group (listed by run detection
-// through its head piece) merges the group's partials in piece order into the
-// head's slot (the team has consumed that partial).
-template <int T, int NV, int V, class Src>
-__global__ void __launch_bounds__(kCombineBlock) k_combine_groups(Src src, int64_t c, float* __restrict__ part,
-                                                                  int64_t nb, int32_t* d_err)
-{
-    pdl_enter();
-    if (read_error(d_err)) return;
-    constexpr int kTeams = kCombineBlock / T;
-    constexpr int CW = T * NV * V;
-    const int lane = threadIdx.x & 31;
-    const int tl = lane & (T - 1);
-    const int64_t team_g = static_cast<int64_t>(blockIdx.x) * kTeams + threadIdx.x / T;
-    const int64_t nteams = static_cast<int64_t>(gridDim.x) * kTeams;
-    const int nchunks = static_cast<int>((c + CW - 1) / CW);
-    const int64_t G = src.count_groups();
-    for (int64_t t = team_g; t < G; t += nteams) {
-        const PieceInfo pc = src.piece(src.group_index(t));
-        int64_t s0, s1;
-        src.seg_bounds(pc.u(), s0, s1);
-        const SplitSegment seg(s0, s1);
-        const int64_t i = seg.index(pc.start);
-        const int64_t K = seg.pieces();
-        const int64_t next = seg.group_head(seg.group(i) + 1);
-        const int64_t cnt = (next < K ? next : K) - i;
-        if (cnt < 2) continue;
-        float* pd = part + part_slot(pc.start, nb) * 2 * c;
-        for (int cc = 0; cc < nchunks; ++cc) {
-            const int64_t col0 = static_cast<int64_t>(cc) * CW;
-            float S[NV][V], C[NV][V];
-            merge_partials<T, NV, V>(part, c, nb, seg, [i](int64_t k) { return i + k; }, cnt, col0, tl, S, C);
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                if (col < c) {
-                    st_part<V>(pd + col, S[k]);
-                    st_part<V>(pd + c + col, C[k]);
-                }
-            }
-        }
-    }
-}
-
-// Second combine stage: one team per split segment merges its groups' pairs in
-// group order (each group's pair sits in its head piece's slot) and applies the
-// update.
+// The split segments, in one launch: one team per combine group (listed by run
+// detection through its head piece) merges the group's partials in piece order
+// into the head's slot, then counts the group in its segment (atomic counter;
+// the pair is released first); the last group of a segment to arrive merges the
+// groups' pairs in group order and applies the update.  The order of every
+// addition is fixed by the slots, whichever team arrives last, and no team
+// waits for another.
 template <int T, int NV, int V, class Src, class Epi>
-__global__ void __launch_bounds__(kCombineBlock) k_combine_final(Src src, int64_t c, Epi epi,
-                                                                 const float* __restrict__ part, int64_t nb,
+__global__ void __launch_bounds__(kCombineBlock) k_combine_split(Src src, int64_t c, Epi epi,
+                                                                 float* __restrict__ part, int64_t nb,
                                                                  int32_t* d_err)
 {
     pdl_enter();
@@ -802,14 +763,43 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_final(Src src, int64_
     const int64_t team_g = static_cast<int64_t>(blockIdx.x) * kTeams + threadIdx.x / T;
     const int64_t nteams = static_cast<int64_t>(gridDim.x) * kTeams;
     const int nchunks = static_cast<int>((c + CW - 1) / CW);
-    const int64_t S_ = src.count_split();
-    for (int64_t t = team_g; t < S_; t += nteams) {
-        const PieceInfo pc = src.piece(src.split_index(t));   // the segment's first piece
+    const int64_t G = src.count_groups();
+    for (int64_t t = team_g; t < G; t += nteams) {
+        const PieceInfo pc = src.piece(src.group_index(t));
         int64_t s0, s1;
         src.seg_bounds(pc.u(), s0, s1);
         const SplitSegment seg(s0, s1);
+        const int64_t i = seg.index(pc.start);
+        const int64_t K = seg.pieces();
+        const int64_t next = seg.group_head(seg.group(i) + 1);
+        const int64_t cnt = (next < K ? next : K) - i;
+        if (cnt > 1) {
+            float* pd = part + part_slot(pc.start, nb) * 2 * c;
+            for (int cc = 0; cc < nchunks; ++cc) {
+                const int64_t col0 = static_cast<int64_t>(cc) * CW;
+                float S[NV][V], C[NV][V];
+                merge_partials<T, NV, V>(part, c, nb, seg, [i](int64_t k) { return i + k; }, cnt, col0, tl, S, C);
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+                    if (col < c) {
+                        st_part<V>(pd + col, S[k]);
+                        st_part<V>(pd + c + col, C[k]);
+                    }
+                }
+            }
+        }
         const int64_t g0 = seg.group(0);
-        const int64_t ng = seg.group(seg.pieces() - 1) - g0 + 1;
+        const int64_t ng = seg.group(K - 1) - g0 + 1;
+        if (ng > 1) {
+            __threadfence();
+            __syncwarp(tmask);
+            uint32_t old = 0;
+            if (tl == 0) old = atomicAdd(src.segment_counter(part_slot(s0, nb)), 1u);
+            old = __shfl_sync(tmask, old, 0, T);
+            if (static_cast<int64_t>(old) != ng - 1) continue;   // another group's team finishes the segment
+            __threadfence();
+        }
         const int64_t* lp = epi.stage_last(pc);
         const int64_t last = lp ? *lp : 0;
         const typename Epi::Row row = epi.make_row(pc, last);
@@ -826,7 +816,7 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_final(Src src, int64_
                 if (col < c) {
                     float g[V];
 #pragma unroll
-                    for (int i = 0; i < V; ++i) g[i] = __fadd_rn(S[k][i], C[k][i]);
+                    for (int e = 0; e < V; ++e) g[e] = __fadd_rn(S[k][e], C[k][e]);
                     epi.template apply<V>(row, col, x[k], g);
                 }
             }
@@ -862,21 +852,13 @@ cudaError_t launch_shape(const Src& src, int64_t max_pieces, int64_t max_split, 
     }
     if (max_split > 0) {
         constexpr int kCTeams = kCombineBlock / T;
-        static const int occ = max_blocks(k_combine_groups<T, NV, V, Src>, kCombineBlock);
+        static const int occ = max_blocks(k_combine_split<T, NV, V, Src, Epi>, kCombineBlock);
         const int64_t cap = static_cast<int64_t>(occ) * num_sms();
-        {
-            SO_PROFILE(Epi::kGroupsName, s);
-            const int64_t groups = nb + nb / kGroup + 2;   // bound on the combine groups
-            const int64_t gb = std::min<int64_t>(cap, (groups + kCTeams - 1) / kCTeams);
-            launch(k_combine_groups<T, NV, V, Src>, dim3(static_cast<unsigned>(gb)), dim3(kCombineBlock), s, src, c, part, nb,
-                                                                                               d_err);
-            const cudaError_t e = cudaGetLastError();
-            if (e != cudaSuccess) return e;
-        }
         SO_PROFILE(Epi::kCombineName, s);
-        const int64_t fb = std::min<int64_t>(cap, (max_split + kCTeams - 1) / kCTeams);
-        launch(k_combine_final<T, NV, V, Src, Epi>, dim3(static_cast<unsigned>(fb)), dim3(kCombineBlock), s, src, c, epi, part, nb,
-                                                                                             d_err);
+        const int64_t groups = nb + nb / kGroup + 2;   // bound on the combine groups
+        const int64_t gb = std::min<int64_t>(cap, (groups + kCTeams - 1) / kCTeams);
+        launch(k_combine_split<T, NV, V, Src, Epi>, dim3(static_cast<unsigned>(gb)), dim3(kCombineBlock), s, src, c,
+               epi, part, nb, d_err);
         return cudaGetLastError();
     }
     return cudaSuccess;
@@ -914,7 +896,7 @@ cudaError_t launch_fused(const Src& src, int64_t max_pieces, int64_t max_split, 
 
 inline SortedSrc sorted_src(const SortWs& ws)
 {
-    return SortedSrc{ws.rec, ws.vals[ws.final_buf], ws.seg_off, ws.mlist, ws.slist, ws.glist, ws.counts};
+    return SortedSrc{ws.rec, ws.vals[ws.final_buf], ws.seg_off, ws.mlist, ws.slist, ws.glist, ws.counts, ws.scnt};
 }
 
 }  // namespace so

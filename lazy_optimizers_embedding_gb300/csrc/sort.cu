@@ -74,6 +74,7 @@ WsLayout ws_layout(int64_t n, int64_t c, int64_t bound)
     L.counts = take(sizeof(uint32_t) * kCountsWords);
     L.rstatus = take(sizeof(uint32_t) * (size_t)L.passes * L.sort_tiles * 256);
     L.dstatus = take(sizeof(unsigned long long) * (size_t)L.run_tiles);
+    L.scnt = take(sizeof(uint32_t) * (size_t)(2 * L.nb));
     L.ctrl_end = align_up(off, 256);
     L.total = L.ctrl_end;
     return L;
@@ -98,6 +99,7 @@ SortWs carve(const WsLayout& L, void* ws)
     w.counts = reinterpret_cast<uint32_t*>(b + L.counts);
     w.rstatus = reinterpret_cast<uint32_t*>(b + L.rstatus);
     w.dstatus = reinterpret_cast<unsigned long long*>(b + L.dstatus);
+    w.scnt = reinterpret_cast<uint32_t*>(b + L.scnt);
     w.final_buf = (L.passes - 1) & 1;
     return w;
 }
