@@ -26,7 +26,15 @@
  *             overlap each other.  Any alignment is accepted; 16-byte aligned
  *             arrays with c % 4 == 0 take the 128-bit vector path.
  *   Streams.  Work is enqueued on `stream` (0 = legacy default stream) and never
- *             synchronises the host.
+ *             synchronises the host.  The library's kernels are launched with
+ *             programmatic dependent launch: each may be scheduled while the
+ *             kernel before it on the stream finishes, and waits for it before
+ *             touching memory that kernel may use.  One exception: on a raw
+ *             (non-canonical) gradient, the first kernel reads the index array
+ *             before that wait, so an index array produced on the same stream
+ *             must not be written by a kernel that itself lets its dependents
+ *             start early (copies, ordinary kernel launches and this library's
+ *             own calls are all fine).
  *   Errors.   Host-checkable problems (null pointer, negative size, bad config,
  *             t < 1, workspace too small, a size beyond a stated limit) return a
  *             non-zero sparse_status_t before anything is enqueued.  A failed

@@ -14,10 +14,11 @@ namespace so {
 
 // ---------------------------------------------------------------- launches
 // Every kernel of this library is launched with programmatic dependent launch
-// allowed, and every kernel starts with pdl_enter(): it waits until the
-// previous kernel on the stream has completed and its memory is visible
-// (griddepcontrol.wait), then lets the next kernel's blocks be scheduled
-// (griddepcontrol.launch_dependents).  Results and stream order are those of
+// allowed, and every kernel calls pdl_enter() before it touches memory another
+// kernel uses (at its start, except the histogram kernel, which first counts
+// the caller's index array): it waits until the previous kernel on the stream
+// has completed and its memory is visible (griddepcontrol.wait), then lets the
+// next kernel's blocks be scheduled (griddepcontrol.launch_dependents).  Results and stream order are those of
 // plain launches; what is saved is the launch latency between dependent
 // kernels, since the next grid is already resident when the wait returns.
 __device__ __forceinline__ void pdl_enter()

@@ -118,11 +118,12 @@ __global__ void __launch_bounds__(kBlock) k_range_hist(const int64_t* __restrict
                                                        uint4* __restrict__ ctrl, uint32_t ctrl_words,
                                                        int32_t* d_err)
 {
-    pdl_enter();
+    // Counting reads only the caller's index array and shared memory, so it runs
+    // before the wait for the previous kernel on the stream (which may still be
+    // using the workspace); the control words and the histograms are written
+    // after it.
     __shared__ uint32_t sh[kMaxPasses * 256];
     for (int i = threadIdx.x; i < kMaxPasses * 256; i += kBlock) sh[i] = 0;
-    for (uint32_t i = blockIdx.x * kBlock + threadIdx.x; i < ctrl_words; i += gridDim.x * kBlock)
-        ctrl[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     int bad = 0;
     const uint32_t stride = gridDim.x * kBlock * kHistItems;
@@ -148,7 +149,11 @@ __global__ void __launch_bounds__(kBlock) k_range_hist(const int64_t* __restrict
             }
         }
     }
-    if (__syncthreads_or(bad) && threadIdx.x == 0) set_error(d_err, SPARSE_ERR_INDEX_OUT_OF_RANGE);
+    const int any_bad = __syncthreads_or(bad);
+    pdl_enter();
+    for (uint32_t i = blockIdx.x * kBlock + threadIdx.x; i < ctrl_words; i += gridDim.x * kBlock)
+        ctrl[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (any_bad && threadIdx.x == 0) set_error(d_err, SPARSE_ERR_INDEX_OUT_OF_RANGE);
     uint32_t* mine = bh + static_cast<size_t>(blockIdx.x) * kMaxPasses * 256;
     for (int i = threadIdx.x; i < passes * 256; i += kBlock) mine[i] = sh[i];
 }
