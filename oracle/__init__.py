@@ -24,6 +24,8 @@ _LIB_PATH = os.path.join(_OUT_DIR, "libsparse_oracle.so")
 
 MODE_LAZY = 0
 MODE_DORMANCY_DECAY = 1
+WD_L2 = 0          # weight decay added to the gradient (classic Adam L2)
+WD_DECOUPLED = 1   # weight decay added to the descent direction (AdamW)
 LS_PER_ROW = 0
 LS_PER_COORD = 1
 FORM_ROW_COO = 0
@@ -62,7 +64,7 @@ def lib():
         l.oracle_row_coo_to_csr.argtypes = [_P, _I64, _I64, _I64, _P, _P]
         l.oracle_adam_table_step.argtypes = [_P, _P, _P, _INT, _P, _INT, _I64, _I64, _INT,
                                              _P, _I64, _INT, _P, _P, _P,
-                                             _I64, _D, _D, _D, _D, _INT]
+                                             _I64, _D, _D, _D, _D, _INT, _D, _INT]
         l.oracle_sgd_table_step.argtypes = [_P, _P, _INT, _I64, _I64, _INT,
                                             _P, _I64, _INT, _P, _P, _P, _D, _D, _D]
         for f in (l.oracle_canonicalize, l.oracle_csr_validate, l.oracle_csr_to_coo,
@@ -160,7 +162,7 @@ def _state_kind(*arrs):
 
 def adam_table_step(p, m, v, last_step, t: int, *, lr, beta1, beta2, eps, mode,
                     rows=None, vals=None, is_canonical=False, row_off=None, cols=None,
-                    ls_per_coord=False) -> int:
+                    ls_per_coord=False, weight_decay=0.0, wd_mode=0) -> int:
     """One lazy Adam step, in place on p, m, v ([r, c] or [r]) and last_step.  Returns the status.
 
     Gradient as row-COO (``rows``, ``vals`` [n, c]) or CSR (``row_off``, ``cols``, ``vals`` [nnz]).
@@ -180,7 +182,7 @@ def adam_table_step(p, m, v, last_step, t: int, *, lr, beta1, beta2, eps, mode,
     return lib().oracle_adam_table_step(
         _ptr(p), _ptr(m), _ptr(v), f64, _ptr(last_step), LS_PER_COORD if ls_per_coord else LS_PER_ROW,
         r, c, form, _ptr(rows), n, int(bool(is_canonical)), _ptr(row_off), _ptr(cols), _ptr(vals),
-        int(t), float(lr), float(beta1), float(beta2), float(eps), int(mode))
+        int(t), float(lr), float(beta1), float(beta2), float(eps), int(mode), float(weight_decay), int(wd_mode))
 
 
 def sgd_table_step(p, buf, *, lr, momentum, weight_decay, rows=None, vals=None,

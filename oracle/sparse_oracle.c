@@ -23,6 +23,10 @@
  *        Aggregation & Sorted I/O" and API step(): duplicate indices are summed,
  *        indices sorted after deduplication; "Validated Inputs": negative or
  *        out-of-range indices are explicit errors.
+ *   [S7] same README, "Explicit Weight Decay Semantics" and the API's
+ *        weight_decay / weight_decay_mode (Euclidean case, k = 0):
+ *        "l2" adds wd*w to the gradient (classic Adam L2); "decoupled" adds
+ *        wd*w to the descent direction (AdamW).
  *
  * Readings where the pages are silent (each is listed in the design doc):
  *   - duplicates are summed in fp64 in input order, starting from the first
@@ -35,7 +39,9 @@
  *     as printed in [S3];
  *   - SGD momentum: buf = mu*buf + g', no dampening, no Nesterov, no mu^gap
  *     catch-up; weight decay coupled: g' = g + wd*p;
- *   - last_step is written (= t) in both Adam modes.
+ *   - last_step is written (= t) in both Adam modes;
+ *   - Adam weight decay, like every other term, acts on touched coordinates only
+ *     and uses the parameter value read at the step (no decay over dormant steps).
  *
  * Arithmetic: every floating-point step in fp64.  State is read from its
  * storage type (fp32, or fp64 for the pin tests) and rounded once on store.
@@ -57,6 +63,7 @@ enum {
 };
 
 enum { OR_MODE_LAZY = 0, OR_MODE_DORMANCY_DECAY = 1 };
+enum { OR_WD_L2 = 0, OR_WD_DECOUPLED = 1 };
 enum { OR_LS_PER_ROW = 0, OR_LS_PER_COORD = 1 };
 enum { OR_FORM_ROW_COO = 0, OR_FORM_CSR = 1 };
 
@@ -326,23 +333,29 @@ static int build_touched(int64_t r, int64_t c, int form, const int64_t* row_idx,
  *     gap = t - last_step[i]                             (>= 1, [S4])
  *     b1, b2 = beta1, beta2                              (Lazy, [S3])
  *     b1, b2 = beta1^gap, beta2^gap                      (DormancyDecay, [S4])
+ *     g  = g + wd*p                                      (wd_mode l2, [S7])
  *     m = b1*m + (1-beta1)*g ;  v = b2*v + (1-beta2)*g^2
  *     m_hat = m / (1 - beta1^t) ;  v_hat = v / (1 - beta2^t)     ([S5])
- *     p -= lr * m_hat / (sqrt(v_hat) + eps)
+ *     p -= lr * m_hat / (sqrt(v_hat) + eps)                       (l2)
+ *     p -= lr * (m_hat / (sqrt(v_hat) + eps) + wd*p)              (wd_mode decoupled, [S7])
  *     last_step[i] = t
+ * with p on the right the value read at the step; wd = 0 is plain lazy Adam.
  * Untouched coordinates are not read or written.
  */
 int oracle_adam_table_step(void* p, void* m, void* v, int state_f64, int64_t* last_step,
                            int ls_layout, int64_t r, int64_t c, int form,
                            const int64_t* row_idx, int64_t n, int is_canonical,
                            const int64_t* row_off, const int32_t* cols, const float* vals,
-                           int64_t t, double lr, double beta1, double beta2, double eps, int mode)
+                           int64_t t, double lr, double beta1, double beta2, double eps, int mode,
+                           double weight_decay, int wd_mode)
 {
     if (r < 0 || c < 1 || t < 1) return OR_ERR_INVALID_ARG;
     if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0)) return OR_ERR_INVALID_ARG;
     if (!(eps > 0.0) || !isfinite(eps) || !isfinite(lr)) return OR_ERR_INVALID_ARG;
     if (mode != OR_MODE_LAZY && mode != OR_MODE_DORMANCY_DECAY) return OR_ERR_INVALID_ARG;
     if (ls_layout != OR_LS_PER_ROW && ls_layout != OR_LS_PER_COORD) return OR_ERR_INVALID_ARG;
+    if (!(weight_decay >= 0.0) || !isfinite(weight_decay)) return OR_ERR_INVALID_ARG;
+    if (wd_mode != OR_WD_L2 && wd_mode != OR_WD_DECOUPLED) return OR_ERR_INVALID_ARG;
 
     touched_t tc;
     int rc = build_touched(r, c, form, row_idx, n, is_canonical, row_off, cols, vals,
@@ -365,7 +378,9 @@ int oracle_adam_table_step(void* p, void* m, void* v, int state_f64, int64_t* la
         const int64_t i = tc.lin[k];
         const int64_t s = last_step[ls_layout == OR_LS_PER_ROW ? tc.row[k] : i];
         const int64_t gap = t - s;
-        const double g = (double)tc.g[k];
+        const double p0 = ld(p, i, state_f64);
+        double g = (double)tc.g[k];
+        if (wd_mode == OR_WD_L2) g += weight_decay * p0;
         double b1 = beta1, b2 = beta2;
         if (mode == OR_MODE_DORMANCY_DECAY) {
             b1 = pow(beta1, (double)gap);
@@ -375,7 +390,9 @@ int oracle_adam_table_step(void* p, void* m, void* v, int state_f64, int64_t* la
         const double vi = b2 * ld(v, i, state_f64) + (1.0 - beta2) * g * g;
         const double m_hat = mi / bc1;
         const double v_hat = vi / bc2;
-        const double pi = ld(p, i, state_f64) - lr * m_hat / (sqrt(v_hat) + eps);
+        double dir = m_hat / (sqrt(v_hat) + eps);
+        if (wd_mode == OR_WD_DECOUPLED) dir += weight_decay * p0;
+        const double pi = p0 - lr * dir;
         st(m, i, mi, state_f64);
         st(v, i, vi, state_f64);
         st(p, i, pi, state_f64);

@@ -153,6 +153,77 @@ def test_p1_dense_adam_reduction_vs_torch():
 
 
 # --------------------------------------------------------------------------
+# P10: weight decay (DSA README, "Explicit Weight Decay Semantics", k = 0)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("wd_mode", [oracle.WD_L2, oracle.WD_DECOUPLED], ids=["l2", "decoupled"])
+def test_p10_weight_decay_vs_torch(wd_mode):
+    """With every coordinate touched every step, "l2" is classic Adam with L2
+    (torch.optim.Adam weight_decay) and "decoupled" is AdamW (torch.optim.AdamW),
+    in both lazy modes."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(12)
+    r, c, T, wd = 4, 3, 20, 0.05
+    hp = dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8)
+    p0 = rng.standard_normal((r, c))
+    grads = rng.standard_normal((T, r, c)).astype(np.float32)
+    out = {}
+    for mode in (LAZY, DD):
+        p, m, v = p0.copy(), np.zeros((r, c)), np.zeros((r, c))
+        ls = np.zeros(r, np.int64)
+        for t in range(1, T + 1):
+            assert oracle.adam_table_step(p, m, v, ls, t, rows=np.arange(r), vals=grads[t - 1], is_canonical=True,
+                                          mode=mode, weight_decay=wd, wd_mode=wd_mode, **hp) == 0
+        out[mode] = p
+    assert out[LAZY].tobytes() == out[DD].tobytes()
+    tp = torch.tensor(p0, dtype=torch.float64, requires_grad=True)
+    cls = torch.optim.Adam if wd_mode == oracle.WD_L2 else torch.optim.AdamW
+    opt = cls([tp], lr=hp["lr"], betas=(hp["beta1"], hp["beta2"]), eps=hp["eps"], weight_decay=wd, foreach=False)
+    for t in range(T):
+        tp.grad = torch.tensor(grads[t].astype(np.float64))
+        opt.step()
+    np.testing.assert_allclose(out[DD], tp.detach().numpy(), rtol=1e-12, atol=1e-15)
+    # the two modes really differ
+    if wd_mode == oracle.WD_DECOUPLED:
+        other = torch.tensor(p0, dtype=torch.float64, requires_grad=True)
+        o2 = torch.optim.Adam([other], lr=hp["lr"], betas=(hp["beta1"], hp["beta2"]), eps=hp["eps"],
+                              weight_decay=wd, foreach=False)
+        for t in range(T):
+            other.grad = torch.tensor(grads[t].astype(np.float64))
+            o2.step()
+        assert np.abs(out[DD] - other.detach().numpy()).max() > 1e-6
+
+
+@pytest.mark.parametrize("wd_mode", [oracle.WD_L2, oracle.WD_DECOUPLED], ids=["l2", "decoupled"])
+def test_p10_weight_decay_touches_only_listed_coordinates(wd_mode):
+    """Decay is lazy: a row left out of a step keeps its bytes, whatever wd."""
+    rng = np.random.default_rng(13)
+    r, c = 6, 2
+    p = rng.standard_normal((r, c)).astype(np.float32)
+    p[5] = [np.float32(-0.0), np.float32(1e-40)]
+    m, v = np.zeros_like(p), np.zeros_like(p)
+    ls = np.zeros(r, np.int64)
+    before = p.copy()
+    for t in range(1, 6):
+        rows = np.array([0, 2, 3], np.int64)
+        g = rng.standard_normal((3, c)).astype(np.float32)
+        assert oracle.adam_table_step(p, m, v, ls, t, rows=rows, vals=g, is_canonical=True, mode=DD, lr=1e-2,
+                                      beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.3, wd_mode=wd_mode) == 0
+    for i in (1, 4, 5):
+        assert p[i].tobytes() == before[i].tobytes()
+    assert not np.array_equal(p[0], before[0])
+
+
+def test_p10_weight_decay_rejects_bad_settings():
+    p = np.zeros((2, 1), np.float32)
+    m, v = np.zeros_like(p), np.zeros_like(p)
+    ls = np.zeros(2, np.int64)
+    kw = dict(rows=np.array([0]), vals=np.ones((1, 1), np.float32), is_canonical=True, mode=DD, lr=1e-2,
+              beta1=0.9, beta2=0.999, eps=1e-8)
+    assert oracle.adam_table_step(p, m, v, ls, 1, weight_decay=-1.0, **kw) == oracle.ERR_INVALID_ARG
+    assert oracle.adam_table_step(p, m, v, ls, 1, weight_decay=0.1, wd_mode=7, **kw) == oracle.ERR_INVALID_ARG
+
+
+# --------------------------------------------------------------------------
 # P2 / P7: dormancy equivalence and brute force against the dense emulator
 # --------------------------------------------------------------------------
 def _random_touches(rng, n, T, density):
