@@ -102,9 +102,23 @@ typedef enum {
     SPARSE_GRAD_CSR = 1      /* CsrGradient: row_off[r+1], cols[nnz], vals[nnz] */
 } sparse_grad_form_t;
 
-/* SparseAdamConfig.  beta1, beta2 in [0, 1); eps > 0; lr finite. */
+/* Adam weight decay ("DiskSparseAdam (DSA)" README, "Explicit Weight Decay
+ * Semantics", Euclidean case): L2 adds weight_decay*p to the gradient (classic
+ * Adam L2); DECOUPLED adds weight_decay*p to the descent direction (AdamW).
+ * Like every other term it acts on touched coordinates only, with the value of
+ * p read at the step (no decay over dormant steps). */
+typedef enum {
+    SPARSE_ADAM_WD_L2 = 0,
+    SPARSE_ADAM_WD_DECOUPLED = 1
+} sparse_adam_wd_mode_t;
+
+/* SparseAdamConfig.  beta1, beta2 in [0, 1); eps > 0; lr finite; weight_decay
+ * >= 0 and finite (0: plain lazy Adam, whatever the mode); weight_decay_mode a
+ * sparse_adam_wd_mode_t. */
 typedef struct {
     double lr, beta1, beta2, eps;
+    double weight_decay;
+    int32_t weight_decay_mode;
 } sparse_adam_config_t;
 
 /* SparseSgdConfig.  momentum >= 0 and weight_decay >= 0, finite; lr finite. */

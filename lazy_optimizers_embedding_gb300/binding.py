@@ -26,6 +26,8 @@ ERR_INTERNAL = 7
 
 LAZY = 0
 DORMANCY_DECAY = 1
+WD_L2 = 0          # sparse_adam_wd_mode_t
+WD_DECOUPLED = 1
 LAST_STEP_PER_ROW = 0
 LAST_STEP_PER_COORD = 1
 GRAD_ROW_COO = 0
@@ -33,9 +35,9 @@ GRAD_CSR = 1
 
 
 class AdamConfig(ctypes.Structure):
-    """sparse_adam_config_t (SparseAdamConfig)."""
+    """sparse_adam_config_t (SparseAdamConfig); weight decay 0 and mode WD_L2 unless given."""
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
-                ("eps", ctypes.c_double)]
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("weight_decay_mode", ctypes.c_int32)]
 
 
 class SgdConfig(ctypes.Structure):

@@ -24,7 +24,8 @@ sparse_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SPARSE_OK :
 bool valid_adam_cfg(const sparse_adam_config_t& c)
 {
     return finite(c.lr) && c.beta1 >= 0.0 && c.beta1 < 1.0 && c.beta2 >= 0.0 && c.beta2 < 1.0 &&
-           c.eps > 0.0 && finite(c.eps);
+           c.eps > 0.0 && finite(c.eps) && finite(c.weight_decay) && c.weight_decay >= 0.0 &&
+           (c.weight_decay_mode == SPARSE_ADAM_WD_L2 || c.weight_decay_mode == SPARSE_ADAM_WD_DECOUPLED);
 }
 
 bool valid_sgd_cfg(const sparse_sgd_config_t& c)
@@ -48,6 +49,9 @@ AdamParams adam_params(float* p, float* m, float* v, int64_t* ls, int ls_per_coo
     P.t = t;
     P.beta1 = static_cast<float>(cfg.beta1);
     P.beta2 = static_cast<float>(cfg.beta2);
+    P.wd = static_cast<float>(cfg.weight_decay);
+    P.wd_lo = static_cast<float>(cfg.weight_decay - static_cast<double>(P.wd));
+    P.wd_decoupled = (cfg.weight_decay_mode == SPARSE_ADAM_WD_DECOUPLED);
     P.omb1 = static_cast<float>(1.0 - cfg.beta1);
     P.omb2 = static_cast<float>(1.0 - cfg.beta2);
     P.log2b1 = cfg.beta1 > 0.0 ? static_cast<float>(std::log2(cfg.beta1)) : -INFINITY;
@@ -68,6 +72,7 @@ SgdParams sgd_params(float* p, float* buf, const sparse_sgd_config_t& cfg)
     P.momentum = static_cast<float>(cfg.momentum);
     P.momentum_lo = static_cast<float>(cfg.momentum - static_cast<double>(P.momentum));
     P.wd = static_cast<float>(cfg.weight_decay);
+    P.wd_lo = static_cast<float>(cfg.weight_decay - static_cast<double>(P.wd));
     P.wd_lo = static_cast<float>(cfg.weight_decay - static_cast<double>(P.wd));
     return P;
 }

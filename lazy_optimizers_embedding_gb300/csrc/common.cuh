@@ -244,6 +244,8 @@ struct AdamParams {
     float log2b1, log2b2; // log2(beta) (-inf for beta = 0)
     float inv_bc1, inv_bc2;  // 1 / (1 - beta^t)
     float lr, eps;
+    float wd, wd_lo;      // weight decay as hi + lo (0: none)
+    int wd_decoupled;     // 1: added to the descent direction (AdamW); 0: to the gradient (L2)
 };
 
 struct SgdParams {

@@ -229,9 +229,29 @@ __device__ __forceinline__ void dormancy_factors(const AdamParams& P, int64_t ga
 
 // m = b1*m + (1-beta1)*g ; v = b2*v + (1-beta2)*g^2 ;
 // p -= lr * (m / (1-beta1^t)) / (sqrt(v / (1-beta2^t)) + eps)
+// With weight decay ("DiskSparseAdam (DSA)" README, "Explicit Weight Decay
+// Semantics"): L2 adds wd*p to g first; decoupled adds wd*p to the descent
+// direction, p -= lr * (m_hat / (sqrt(v_hat) + eps) + wd*p) (AdamW).
 __device__ __forceinline__ void adam_coord(const AdamParams& P, float b1, float b2, float g, float& p,
                                            float& m, float& v)
 {
+    if (P.wd != 0.0f) {
+        const float p0 = p;
+        // L2: g + wd*p with wd as a hi + lo pair, so that a gradient nearly cancelled by
+        // the decay term keeps its relative accuracy (the product is exact inside the FMA)
+        if (!P.wd_decoupled) g = __fmaf_rn(P.wd_lo, p0, __fmaf_rn(P.wd, p0, g));
+        const float mi = __fmaf_rn(b1, m, __fmul_rn(P.omb1, g));
+        const float vi = __fmaf_rn(b2, v, __fmul_rn(P.omb2, __fmul_rn(g, g)));
+        const float m_hat = __fmul_rn(mi, P.inv_bc1);
+        const float v_hat = __fmul_rn(vi, P.inv_bc2);
+        const float denom = __fadd_rn(__fsqrt_rn(v_hat), P.eps);
+        float dir = __fdiv_rn(m_hat, denom);
+        if (P.wd_decoupled) dir = __fmaf_rn(P.wd, p0, dir);
+        p = __fsub_rn(p0, __fmul_rn(P.lr, dir));
+        m = mi;
+        v = vi;
+        return;
+    }
     const float mi = __fmaf_rn(b1, m, __fmul_rn(P.omb1, g));
     const float vi = __fmaf_rn(b2, v, __fmul_rn(P.omb2, __fmul_rn(g, g)));
     const float m_hat = __fmul_rn(mi, P.inv_bc1);

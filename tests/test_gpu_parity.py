@@ -118,6 +118,9 @@ def _run_adam(so, R, c, steps, mode, gen, form, layout=None, hp=ADAM, check_ever
     op, om, ov, ols = p0.copy(), np.zeros_like(p0), np.zeros_like(p0), np.zeros(ls_n, np.int64)
     err = so.error_word()
     cfg = so.AdamConfig(**hp)
+    ohp = dict(hp)   # the oracle names the weight-decay mode wd_mode
+    if "weight_decay_mode" in ohp:
+        ohp["wd_mode"] = ohp.pop("weight_decay_mode")
     omode = oracle.MODE_DORMANCY_DECAY if mode == so.DORMANCY_DECAY else oracle.MODE_LAZY
     touched = np.zeros((R, c), bool)
     ws = None
@@ -132,7 +135,7 @@ def _run_adam(so, R, c, steps, mode, gen, form, layout=None, hp=ADAM, check_ever
             so.check(so.sparse_adam_table_step(p, m, v, ls, layout or so.LAST_STEP_PER_ROW, R, c, grad, t, cfg, mode,
                                                ws, err), "adam_table_step")
             rc = oracle.adam_table_step(op, om, ov, ols, t, rows=rows, vals=vals, is_canonical=(form == "canon"),
-                                        mode=omode, ls_per_coord=per_coord, **hp)
+                                        mode=omode, ls_per_coord=per_coord, **ohp)
             touched[np.unique(rows)] = True
         else:
             row_off, cols, vals = g
@@ -140,7 +143,7 @@ def _run_adam(so, R, c, steps, mode, gen, form, layout=None, hp=ADAM, check_ever
             so.check(so.sparse_adam_table_step(p, m, v, ls, layout, R, c, grad, t, cfg, mode, None, err),
                      "adam_table_step csr")
             rc = oracle.adam_table_step(op, om, ov, ols, t, row_off=row_off, cols=cols, vals=vals, mode=omode,
-                                        ls_per_coord=per_coord, **hp)
+                                        ls_per_coord=per_coord, **ohp)
             rr = np.repeat(np.arange(R), np.diff(row_off))
             touched[rr, cols] = True
         assert rc == 0
@@ -228,6 +231,48 @@ def test_adam_csr_full_rows_per_row_last_step(cuda_lib, mode):
         return ro, co, rng.standard_normal(rows.shape[0] * c).astype(np.float32)
 
     _run_adam(so, R, c, 5, mode, gen, "csr", layout=so.LAST_STEP_PER_ROW, check_every=True)
+
+
+@pytest.mark.parametrize("wd_mode", [0, 1], ids=["l2", "decoupled"])
+@pytest.mark.parametrize("mode", [0, 1], ids=["lazy", "dormancy_decay"])
+@pytest.mark.parametrize("form", ["raw", "canon", "csr_elem", "csr_full"])
+def test_adam_weight_decay(cuda_lib, wd_mode, mode, form):
+    """DSA's weight-decay modes on every gradient form, touched coordinates only."""
+    so = cuda_lib
+    hp = dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.05, weight_decay_mode=wd_mode)
+    R, c = 3000, 64
+
+    def gen(s):
+        rng = np.random.default_rng(7000 + s)
+        if form == "raw":
+            rows = _raw_rows(rng, 2500, R, hot=5, hot_count=900) % max(1, R // (1 + s % 2))
+            return rows, (rng.standard_normal((rows.shape[0], c)) * 0.01).astype(np.float32)
+        if form == "canon":
+            rows = np.sort(rng.choice(R, size=R // 4, replace=False)).astype(np.int64)
+            return rows, rng.standard_normal((rows.shape[0], c)).astype(np.float32)
+        if form == "csr_elem":
+            return _csr_elem(rng, R, c, 400, 9)
+        rows = np.sort(rng.choice(R, size=500, replace=False))
+        ro, co = oracle.row_coo_to_csr(rows, R, c)
+        return ro, co, rng.standard_normal(rows.shape[0] * c).astype(np.float32)
+
+    f = "csr" if form.startswith("csr") else form
+    layout = so.LAST_STEP_PER_COORD if form == "csr_elem" else so.LAST_STEP_PER_ROW
+    _run_adam(so, R, c, 4, mode, gen, f, layout=layout, hp=hp, check_every=True)
+
+
+def test_adam_weight_decay_bad_settings_rejected(cuda_lib):
+    import torch
+    so = cuda_lib
+    p = torch.zeros((4, 4), device="cuda")
+    m, v = torch.zeros_like(p), torch.zeros_like(p)
+    ls = torch.zeros(4, dtype=torch.int64, device="cuda")
+    g = so.row_coo(dev(np.array([1], np.int64)), dev(np.ones((1, 4), np.float32)), True)
+    err = so.error_word()
+    for kw in (dict(weight_decay=-0.1), dict(weight_decay=float("nan")), dict(weight_decay=0.1, weight_decay_mode=5)):
+        cfg = so.AdamConfig(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, **kw)
+        assert so.sparse_adam_table_step(p, m, v, ls, so.LAST_STEP_PER_ROW, 4, 4, g, 1, cfg, so.DORMANCY_DECAY,
+                                         None, err) == so.ERR_INVALID_ARG
 
 
 def test_summed_lookups_to_csr_then_step(cuda_lib):
