@@ -65,6 +65,8 @@ def lib():
         l.oracle_adam_table_step.argtypes = [_P, _P, _P, _INT, _P, _INT, _I64, _I64, _INT,
                                              _P, _I64, _INT, _P, _P, _P,
                                              _I64, _D, _D, _D, _D, _INT, _D, _INT]
+        l.oracle_read_rows.argtypes = [_P, _I64, _I64, _P, _I64, _P]
+        l.oracle_read_rows.restype = _INT
         l.oracle_sgd_table_step.argtypes = [_P, _P, _INT, _I64, _I64, _INT,
                                             _P, _I64, _INT, _P, _P, _P, _D, _D, _D]
         for f in (l.oracle_canonicalize, l.oracle_csr_validate, l.oracle_csr_to_coo,
@@ -183,6 +185,21 @@ def adam_table_step(p, m, v, last_step, t: int, *, lr, beta1, beta2, eps, mode,
         _ptr(p), _ptr(m), _ptr(v), f64, _ptr(last_step), LS_PER_COORD if ls_per_coord else LS_PER_ROW,
         r, c, form, _ptr(rows), n, int(bool(is_canonical)), _ptr(row_off), _ptr(cols), _ptr(vals),
         int(t), float(lr), float(beta1), float(beta2), float(eps), int(mode), float(weight_decay), int(wd_mode))
+
+
+def read_rows(table, idx, *, check=True):
+    """The rows of a [r, c] fp32 table at the given indices, bit for bit ([n, c])."""
+    table = _c(table, np.float32)
+    r = table.shape[0]
+    c = 1 if table.ndim == 1 else table.shape[1]
+    idx = _c(idx, np.int64)
+    out = np.empty((idx.shape[0], c), np.float32)
+    rc = lib().oracle_read_rows(_ptr(table), r, c, _ptr(idx), idx.shape[0], _ptr(out))
+    if rc:
+        if check:
+            raise OracleError(rc, "read_rows")
+        return rc
+    return out
 
 
 def sgd_table_step(p, buf, *, lr, momentum, weight_decay, rows=None, vals=None,

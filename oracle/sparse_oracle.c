@@ -23,6 +23,8 @@
  *        Aggregation & Sorted I/O" and API step(): duplicate indices are summed,
  *        indices sorted after deduplication; "Validated Inputs": negative or
  *        out-of-range indices are explicit errors.
+ *   [S8] same README, API read_rows(indices): the rows of the table at the given
+ *        indices (the lookup that feeds the forward pass), indices validated.
  *   [S7] same README, "Explicit Weight Decay Semantics" and the API's
  *        weight_decay / weight_decay_mode (Euclidean case, k = 0):
  *        "l2" adds wd*w to the gradient (classic Adam L2); "decoupled" adds
@@ -444,5 +446,24 @@ int oracle_sgd_table_step(void* p, void* buf, int state_f64, int64_t r, int64_t 
         }
     }
     touched_free(&tc);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* row gather [S8]                                                     */
+/* ------------------------------------------------------------------ */
+
+/*
+ * out[i*c .. i*c + c) = table[idx[i]*c .. idx[i]*c + c) for i < n, copied value by
+ * value (bit for bit).  Every index is checked first (0 <= idx[i] < r); on a bad
+ * index nothing is written.
+ */
+int oracle_read_rows(const float* table, int64_t r, int64_t c, const int64_t* idx, int64_t n, float* out)
+{
+    if (r < 0 || c < 1 || n < 0) return OR_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        if (idx[i] < 0 || idx[i] >= r) return OR_ERR_INDEX_OUT_OF_RANGE;
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t k = 0; k < c; ++k) out[i * c + k] = table[idx[i] * c + k];
     return OR_OK;
 }

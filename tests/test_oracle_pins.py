@@ -573,3 +573,27 @@ def test_zero_work_is_noop():
     assert oracle.adam_table_step(p, m, v, ls, 1, rows=np.zeros(0, np.int64), vals=np.zeros((0, 2), np.float32),
                                   lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, mode=DD) == 0
     assert p.tobytes() == snap.tobytes() and not ls.any()
+
+
+# --------------------------------------------------------------------------
+# P11: row gather (DSA README, read_rows)
+# --------------------------------------------------------------------------
+def test_p11_read_rows_equals_fancy_indexing_bitwise():
+    """The gather is numpy fancy indexing, bit for bit (NaN payloads, -0.0, denormals)."""
+    rng = np.random.default_rng(21)
+    t = rng.standard_normal((50, 7)).astype(np.float32)
+    t.view(np.uint32)[3, 2] = 0x7FC01234          # a NaN with a payload
+    t[4, 0], t[4, 1] = np.float32(-0.0), np.float32(1e-42)
+    idx = rng.integers(0, 50, 300)
+    idx[:4] = [3, 4, 49, 0]
+    got = oracle.read_rows(t, idx)
+    assert got.tobytes() == t[idx].tobytes()
+    assert oracle.read_rows(t, np.zeros(0, np.int64)).shape == (0, 7)
+    one_d = rng.standard_normal(9).astype(np.float32)
+    assert oracle.read_rows(one_d, np.array([8, 1])).reshape(-1).tobytes() == one_d[[8, 1]].tobytes()
+
+
+def test_p11_read_rows_rejects_bad_indices():
+    t = np.zeros((5, 2), np.float32)
+    assert oracle.read_rows(t, np.array([0, 5]), check=False) == ERR_INDEX_OUT_OF_RANGE
+    assert oracle.read_rows(t, np.array([-1]), check=False) == ERR_INDEX_OUT_OF_RANGE
