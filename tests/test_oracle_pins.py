@@ -595,5 +595,5 @@ def test_p11_read_rows_equals_fancy_indexing_bitwise():
 
 def test_p11_read_rows_rejects_bad_indices():
     t = np.zeros((5, 2), np.float32)
-    assert oracle.read_rows(t, np.array([0, 5]), check=False) == ERR_INDEX_OUT_OF_RANGE
-    assert oracle.read_rows(t, np.array([-1]), check=False) == ERR_INDEX_OUT_OF_RANGE
+    assert oracle.read_rows(t, np.array([0, 5]), check=False) == oracle.ERR_INDEX_OUT_OF_RANGE
+    assert oracle.read_rows(t, np.array([-1]), check=False) == oracle.ERR_INDEX_OUT_OF_RANGE
