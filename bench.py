@@ -416,6 +416,8 @@ WORKLOADS = {
     "d1_lazy": (wl.CFG_1D, "lazy"), "d1_dd": (wl.CFG_1D, "dd"), "d1_sgd": (wl.CFG_1D_SGD, None),
     "zipf1m_csr": (wl.CFG_ZIPF_1M_64, "dd"), "csr4m": (wl.CFG_CSR_4M_256, "dd"),
     "sgd50m": (wl.CFG_SGD_50M_32, None),
+    # the forward-side row gather (read_rows) of the 10M x 128 table at the Zipf lookups
+    "gather10m": (wl.CFG_ZIPF_10M_128, "gather"),
 }
 
 
@@ -455,6 +457,12 @@ def run_workload(args):
             u = uidx.shape[0]
             units.append(u * c)
             nbytes.append(u * c * 24 + u * 16 + u * c * 8 + (w.rows + 1) * 8)
+        elif mode == "gather":
+            idx = wl.step_indices(w, b)
+            host.append(("gather", idx))
+            units.append(idx.shape[0] * c)
+            # distinct table rows read once (repeats are L2 hits), every output row written, indices read
+            nbytes.append(int(np.unique(idx).shape[0]) * c * 4 + idx.shape[0] * (c * 4 + 8))
         else:
             idx, vals = wl.coo_step(w, b)
             host.append(("coo", idx, vals))
@@ -466,15 +474,23 @@ def run_workload(args):
     p = torch.from_numpy(p0).to(dev).reshape(-1)
     err = so.error_word(dev)
     m = v = ls = buf = None
-    if sgd:
+    if mode == "gather":
+        pass
+    elif sgd:
         buf = torch.zeros_like(p)
     else:
         m, v = torch.zeros_like(p), torch.zeros_like(p)
         ls = torch.zeros(p.numel() if (c == 1 or w.index_dist == "csr_elem") else w.rows, dtype=torch.int64,
                          device=dev)
     dev_in, grads, ws = [], [], None
+    gather_out = None
     for h in host:
-        if h[0] == "csr":
+        if h[0] == "gather":
+            dev_in.append((torch.from_numpy(h[1]).to(dev),))
+            grads.append(None)
+            if gather_out is None:
+                gather_out = torch.empty((h[1].shape[0], c), dtype=torch.float32, device=dev)
+        elif h[0] == "csr":
             t3 = tuple(torch.from_numpy(a).to(dev) for a in h[1:])
             dev_in.append(t3)
             grads.append(so.csr(*t3))
@@ -493,7 +509,10 @@ def run_workload(args):
 
     def step(b):
         state["t"] += 1
-        if c == 1:
+        if mode == "gather":
+            i = dev_in[b][0]
+            rc = so.sparse_read_rows(p, w.rows, c, i, i.numel(), gather_out, err, stream)
+        elif c == 1:
             i, g = dev_in[b]
             if sgd:
                 rc = so.sparse_sgd_step(p, buf, w.rows, i, g, i.numel(), 1, scfg, None, err, stream)
@@ -541,7 +560,9 @@ def run_workload(args):
     if not args.no_cpu_baseline:
         hp = p0.reshape(-1).copy() if c == 1 else p0.copy()
         hm = hv = hls = hbuf = None
-        if sgd:
+        if mode == "gather":
+            pass
+        elif sgd:
             hbuf = np.zeros_like(hp)
         else:
             hm, hv = np.zeros_like(hp), np.zeros_like(hp)
@@ -550,7 +571,10 @@ def run_workload(args):
         for k in range(K + W):
             h = host[order[k]]
             t0 = time.perf_counter()
-            if sgd and c == 1:
+            if mode == "gather":
+                oracle.read_rows(hp, h[1])
+                rc = 0
+            elif sgd and c == 1:
                 rc = oracle.sgd_step(hp, hbuf, h[1], h[2].reshape(-1), lr=w.lr, momentum=w.momentum,
                                      weight_decay=w.weight_decay)
             elif sgd:

@@ -242,6 +242,19 @@ sparse_status_t sparse_sgd_table_step(float* p, float* buf, int64_t r, int64_t c
                                       size_t ws_bytes, int32_t* d_err, cudaStream_t stream);
 
 /*
+ * sparse_read_rows -- the rows of a table at the given indices ("DiskSparseAdam
+ * (DSA)" README, API read_rows(indices): the lookup that feeds the forward pass,
+ * indices validated).
+ *   table: r x c fp32 row-major; idx: n int64 (any order, repeats allowed);
+ *   out:   n x c fp32, out[i*c + k] = table[idx[i]*c + k], copied bit for bit.
+ *   An index outside [0, r) sets *d_err = SPARSE_ERR_INDEX_OUT_OF_RANGE and its
+ *   output row is left unwritten (the other rows are still copied).  n = 0 is a
+ *   no-op.  table and out must not overlap.
+ */
+sparse_status_t sparse_read_rows(const float* table, int64_t r, int64_t c, const int64_t* idx, int64_t n, float* out,
+                                 int32_t* d_err, cudaStream_t stream);
+
+/*
  * sparse_canonicalize_static_ws -- sparse_canonicalize without a caller workspace
  * (no counterpart on the pages: this serves callers, not the method).
  *

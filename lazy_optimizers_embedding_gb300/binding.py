@@ -77,6 +77,7 @@ def _load():
         "sparse_sgd_step": (INT, [P, P, I64, P, P, I64, INT, SgdConfig, P, SZ, P, P]),
         "sparse_sgd_table_step": (INT, [P, P, I64, I64, ctypes.POINTER(Grad), SgdConfig, P, SZ, P, P]),
         "sparse_canonicalize_static_ws": (INT, [P, P, I64, I64, I64, P, P, P, P, P, P, P]),
+        "sparse_read_rows": (INT, [P, I64, I64, P, I64, P, P, P]),
         "sparse_profile_enable": (None, [INT]),
         "sparse_profile_reset": (None, []),
         "sparse_profile_read": (INT, [INT, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_int64),
@@ -93,7 +94,7 @@ LIB = _load()
 EXPORTED = ("sparse_workspace_size", "sparse_status_string", "sparse_canonicalize", "sparse_csr_to_coo",
             "sparse_coo_to_csr", "sparse_row_coo_to_csr", "sparse_adam_step", "sparse_adam_table_step",
             "sparse_sgd_step", "sparse_sgd_table_step", "sparse_canonicalize_static_ws", "sparse_profile_enable",
-            "sparse_profile_reset", "sparse_profile_read")
+            "sparse_profile_reset", "sparse_profile_read", "sparse_read_rows")
 STATIC_WS_BYTES = 16 * 1024 * 1024  # SPARSE_STATIC_WS_BYTES
 
 
@@ -254,6 +255,12 @@ def sparse_sgd_table_step(p, buf, r, c, grad: Grad, cfg: SgdConfig, ws, d_err, s
     return LIB.sparse_sgd_table_step(_ptr(p, torch.float32, "p"), _ptr(buf, torch.float32, "buf"), int(r),
                                      int(c), ctypes.byref(grad), cfg, wp, wb, _ptr(d_err, torch.int32, "d_err"),
                                      _stream(stream))
+
+
+def sparse_read_rows(table, r, c, idx, n, out, d_err, stream=None) -> int:
+    return LIB.sparse_read_rows(_ptr(table, torch.float32, "table"), int(r), int(c), _ptr(idx, torch.int64, "idx"),
+                                int(n), _ptr(out, torch.float32, "out"), _ptr(d_err, torch.int32, "d_err"),
+                                _stream(stream))
 
 
 # ------------------------------------------------------------------ diagnostics

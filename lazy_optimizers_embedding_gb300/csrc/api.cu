@@ -296,4 +296,15 @@ sparse_status_t sparse_sgd_step(float* p, float* buf, int64_t dim, const int64_t
     return sparse_sgd_table_step(p, buf, dim, 1, &grad, cfg, ws, ws_bytes, d_err, stream);
 }
 
+sparse_status_t sparse_read_rows(const float* table, int64_t r, int64_t c, const int64_t* idx, int64_t n, float* out,
+                                 int32_t* d_err, cudaStream_t stream)
+{
+    if (r < 0 || c < 1 || n < 0 || d_err == nullptr) return SPARSE_ERR_INVALID_ARG;
+    if (r > 0 && c > INT64_MAX / r) return SPARSE_ERR_INVALID_ARG;
+    if (n == 0) return SPARSE_OK;
+    if (idx == nullptr || out == nullptr || (r > 0 && table == nullptr)) return SPARSE_ERR_INVALID_ARG;
+    const int vec4 = (c % 4 == 0) && aligned16(table) && aligned16(out);
+    return from_cuda(read_rows(table, r, c, idx, n, out, vec4, d_err, stream));
+}
+
 }  // extern "C"

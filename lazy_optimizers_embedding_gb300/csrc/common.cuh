@@ -276,6 +276,8 @@ cudaError_t fused_rows_store_sorted(const SortWs& ws, const WsLayout& L, const f
 cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, int64_t c, int64_t nnz,
                       int full_rows, const int64_t* ls, int ls_per_coord, int64_t t, int32_t* d_err,
                       cudaStream_t s);
+cudaError_t read_rows(const float* table, int64_t r, int64_t c, const int64_t* idx, int64_t n, float* out, int vec4,
+                      int32_t* d_err, cudaStream_t s);
 cudaError_t csr_adam(const int64_t* row_off, const int32_t* cols, const float* vals, int64_t r,
                      int64_t c, int64_t nnz, const AdamParams& P, int32_t* d_err, cudaStream_t s);
 cudaError_t csr_sgd(const int64_t* row_off, const int32_t* cols, const float* vals, int64_t r,

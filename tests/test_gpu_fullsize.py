@@ -197,3 +197,21 @@ def test_csr_adam_fullsize(cuda_lib, cfg):
     assert tmask.any() and (~tmask).any()
     del p, m, v, ls
     _free()
+
+
+def test_read_rows_10Mx128_zipf_fullsize(cuda_lib):
+    """The forward gather of the 10M x 128 table at one step's 262,144 Zipf lookups, bit for bit."""
+    import torch
+    so = cuda_lib
+    w = wl.CFG_ZIPF_10M_128
+    p0 = wl.table_init(w, threads=16)
+    idx = wl.step_indices(w, 0)
+    out = torch.empty((idx.shape[0], w.cols), dtype=torch.float32, device="cuda")
+    err = so.error_word()
+    t = dev(p0)
+    so.check(so.sparse_read_rows(t, w.rows, w.cols, dev(idx), idx.shape[0], out, err), "read_rows")
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert host(out).tobytes() == oracle.read_rows(p0, idx).tobytes()
+    del t, out
+    _free()

@@ -626,3 +626,42 @@ def test_edge_betas_and_long_gaps(cuda_lib, beta1, gap_steps):
         outs[mode] = host(p)
     if gap_steps == 1:  # every touch has gap 1: the two modes coincide bit for bit
         assert outs[so.LAZY].tobytes() == outs[so.DORMANCY_DECAY].tobytes()
+
+
+# ------------------------------------------------------------------ row gather (read_rows)
+@pytest.mark.parametrize("r,c,n", [(1, 1, 1), (50, 3, 500), (1000, 4, 4097), (3000, 64, 10_000), (2000, 128, 7001),
+                                   (400, 300, 999), (100, 1000, 257)])
+def test_read_rows_bitwise(cuda_lib, r, c, n):
+    import torch
+    so = cuda_lib
+    rng = np.random.default_rng(r * 7 + c)
+    t = rng.standard_normal((r, c)).astype(np.float32)
+    t.view(np.uint32)[0, 0] = 0x7FC0BEEF        # NaN payload
+    if c > 2:
+        t[r - 1, 1], t[r - 1, 2] = np.float32(-0.0), np.float32(3e-41)
+    idx = rng.integers(0, r, n).astype(np.int64)
+    idx[: min(n, 3)] = [0, r - 1, 0][: min(n, 3)]
+    out = torch.full((n, c), 7.0, device="cuda")
+    err = so.error_word()
+    so.check(so.sparse_read_rows(dev(t), r, c, dev(idx), n, out, err), "read_rows")
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert host(out).tobytes() == oracle.read_rows(t, idx).tobytes()
+
+
+def test_read_rows_bad_index_and_empty(cuda_lib):
+    import torch
+    so = cuda_lib
+    t = np.arange(40, dtype=np.float32).reshape(10, 4)
+    idx = np.array([2, 10, 5, -1, 9], np.int64)
+    out = torch.full((5, 4), -3.0, device="cuda")
+    err = so.error_word()
+    so.check(so.sparse_read_rows(dev(t), 10, 4, dev(idx), 5, out, err), "read_rows")
+    torch.cuda.synchronize()
+    assert int(err.item()) == so.ERR_INDEX_OUT_OF_RANGE
+    got = host(out)
+    assert np.array_equal(got[[0, 2, 4]], t[[2, 5, 9]])
+    assert np.all(got[[1, 3]] == -3.0)
+    err2 = so.error_word()
+    assert so.sparse_read_rows(dev(t), 10, 4, dev(idx), 0, out, err2) == so.OK
+    assert so.sparse_read_rows(dev(t), 10, 0, dev(idx), 5, out, err2) == so.ERR_INVALID_ARG
