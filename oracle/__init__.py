@@ -32,6 +32,7 @@ FORM_ROW_COO = 0
 FORM_CSR = 1
 
 OK, ERR_INVALID_ARG, ERR_INDEX_OUT_OF_RANGE, ERR_NOT_CANONICAL, ERR_STEP_ORDER = 0, 1, 2, 3, 4
+ERR_NON_FINITE = 8
 
 
 def build(force: bool = False) -> str:
@@ -66,6 +67,8 @@ def lib():
                                              _P, _I64, _INT, _P, _P, _P,
                                              _I64, _D, _D, _D, _D, _INT, _D, _INT]
         l.oracle_read_rows.argtypes = [_P, _I64, _I64, _P, _I64, _P]
+        l.oracle_check_finite.argtypes = [_P, _I64]
+        l.oracle_check_finite.restype = _INT
         l.oracle_read_rows.restype = _INT
         l.oracle_sgd_table_step.argtypes = [_P, _P, _INT, _I64, _I64, _INT,
                                             _P, _I64, _INT, _P, _P, _P, _D, _D, _D]
@@ -185,6 +188,12 @@ def adam_table_step(p, m, v, last_step, t: int, *, lr, beta1, beta2, eps, mode,
         _ptr(p), _ptr(m), _ptr(v), f64, _ptr(last_step), LS_PER_COORD if ls_per_coord else LS_PER_ROW,
         r, c, form, _ptr(rows), n, int(bool(is_canonical)), _ptr(row_off), _ptr(cols), _ptr(vals),
         int(t), float(lr), float(beta1), float(beta2), float(eps), int(mode), float(weight_decay), int(wd_mode))
+
+
+def check_finite(vals) -> int:
+    """ERR_NON_FINITE when any value is NaN or infinite, else OK."""
+    vals = _c(vals, np.float32)
+    return lib().oracle_check_finite(_ptr(vals), vals.size)
 
 
 def read_rows(table, idx, *, check=True):

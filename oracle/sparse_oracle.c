@@ -23,6 +23,8 @@
  *        Aggregation & Sorted I/O" and API step(): duplicate indices are summed,
  *        indices sorted after deduplication; "Validated Inputs": negative or
  *        out-of-range indices are explicit errors.
+ *   [S9] same README, "Validated Inputs": non-finite gradients are an explicit
+ *        error.
  *   [S8] same README, API read_rows(indices): the rows of the table at the given
  *        indices (the lookup that feeds the forward pass), indices validated.
  *   [S7] same README, "Explicit Weight Decay Semantics" and the API's
@@ -61,7 +63,8 @@ enum {
     OR_ERR_INDEX_OUT_OF_RANGE = 2,
     OR_ERR_NOT_CANONICAL = 3,
     OR_ERR_STEP_ORDER = 4,
-    OR_ERR_NO_MEMORY = 8
+    OR_ERR_NON_FINITE = 8,
+    OR_ERR_NO_MEMORY = 100
 };
 
 enum { OR_MODE_LAZY = 0, OR_MODE_DORMANCY_DECAY = 1 };
@@ -465,5 +468,18 @@ int oracle_read_rows(const float* table, int64_t r, int64_t c, const int64_t* id
         if (idx[i] < 0 || idx[i] >= r) return OR_ERR_INDEX_OUT_OF_RANGE;
     for (int64_t i = 0; i < n; ++i)
         for (int64_t k = 0; k < c; ++k) out[i * c + k] = table[idx[i] * c + k];
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* gradient validation [S9]                                            */
+/* ------------------------------------------------------------------ */
+
+/* OR_ERR_NON_FINITE when any of the n values is NaN or infinite, else OK. */
+int oracle_check_finite(const float* vals, int64_t n)
+{
+    if (n < 0) return OR_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        if (!isfinite(vals[i])) return OR_ERR_NON_FINITE;
     return OR_OK;
 }

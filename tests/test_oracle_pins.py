@@ -597,3 +597,20 @@ def test_p11_read_rows_rejects_bad_indices():
     t = np.zeros((5, 2), np.float32)
     assert oracle.read_rows(t, np.array([0, 5]), check=False) == oracle.ERR_INDEX_OUT_OF_RANGE
     assert oracle.read_rows(t, np.array([-1]), check=False) == oracle.ERR_INDEX_OUT_OF_RANGE
+
+
+# --------------------------------------------------------------------------
+# P12: non-finite gradients (DSA README, "Validated Inputs")
+# --------------------------------------------------------------------------
+def test_p12_check_finite():
+    rng = np.random.default_rng(31)
+    g = rng.standard_normal((100, 8)).astype(np.float32)
+    g[7, 3] = np.float32(3.4e38)                 # large but finite
+    g[8, 1] = np.float32(1e-45)                  # denormal
+    assert oracle.check_finite(g) == oracle.OK
+    assert oracle.check_finite(np.zeros(0, np.float32)) == oracle.OK
+    for bad in (np.nan, np.inf, -np.inf):
+        h = g.copy()
+        h[99, 7] = bad
+        assert oracle.check_finite(h) == oracle.ERR_NON_FINITE
+        assert oracle.check_finite(h) == (oracle.ERR_NON_FINITE if not np.isfinite(h).all() else oracle.OK)
