@@ -81,7 +81,8 @@ typedef enum {
     SPARSE_ERR_STEP_ORDER = 4,         /* device: t <= last_step of a touched coordinate */
     SPARSE_ERR_WORKSPACE = 5,          /* host: ws missing, misaligned or too small */
     SPARSE_ERR_CUDA = 6,               /* host: a CUDA launch or runtime call failed */
-    SPARSE_ERR_INTERNAL = 7            /* device: a bounded wait between thread blocks gave up */
+    SPARSE_ERR_INTERNAL = 7,           /* device: a bounded wait between thread blocks gave up */
+    SPARSE_ERR_NON_FINITE = 8          /* device: a gradient value is NaN or infinite (sparse_check_finite) */
 } sparse_status_t;
 
 /* "Lazy Adam": LazyAdamMode::Lazy and LazyAdamMode::DormancyDecay. */
@@ -240,6 +241,17 @@ sparse_status_t sparse_sgd_step(float* p, float* buf, int64_t dim, const int64_t
 sparse_status_t sparse_sgd_table_step(float* p, float* buf, int64_t r, int64_t c,
                                       const sparse_grad_t* grad, sparse_sgd_config_t cfg, void* ws,
                                       size_t ws_bytes, int32_t* d_err, cudaStream_t stream);
+
+/*
+ * sparse_check_finite -- optional validation of gradient values ("DiskSparseAdam
+ * (DSA)" README, "Validated Inputs": non-finite gradients are an explicit error).
+ *   vals: n fp32 values (a gradient's value array: n = entries x c for row-COO,
+ *   nnz for CSR).  Any NaN or infinity sets *d_err = SPARSE_ERR_NON_FINITE.
+ *   Enqueued before a step on the same stream with the same d_err, it makes that
+ *   step write no state when a value is not finite (the error word is sticky).
+ *   Reads the values once (4 bytes each); n = 0 is a no-op.
+ */
+sparse_status_t sparse_check_finite(const float* vals, int64_t n, int32_t* d_err, cudaStream_t stream);
 
 /*
  * sparse_read_rows -- the rows of a table at the given indices ("DiskSparseAdam

@@ -23,6 +23,7 @@ ERR_STEP_ORDER = 4
 ERR_WORKSPACE = 5
 ERR_CUDA = 6
 ERR_INTERNAL = 7
+ERR_NON_FINITE = 8
 
 LAZY = 0
 DORMANCY_DECAY = 1
@@ -78,6 +79,7 @@ def _load():
         "sparse_sgd_table_step": (INT, [P, P, I64, I64, ctypes.POINTER(Grad), SgdConfig, P, SZ, P, P]),
         "sparse_canonicalize_static_ws": (INT, [P, P, I64, I64, I64, P, P, P, P, P, P, P]),
         "sparse_read_rows": (INT, [P, I64, I64, P, I64, P, P, P]),
+        "sparse_check_finite": (INT, [P, I64, P, P]),
         "sparse_profile_enable": (None, [INT]),
         "sparse_profile_reset": (None, []),
         "sparse_profile_read": (INT, [INT, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_int64),
@@ -94,7 +96,7 @@ LIB = _load()
 EXPORTED = ("sparse_workspace_size", "sparse_status_string", "sparse_canonicalize", "sparse_csr_to_coo",
             "sparse_coo_to_csr", "sparse_row_coo_to_csr", "sparse_adam_step", "sparse_adam_table_step",
             "sparse_sgd_step", "sparse_sgd_table_step", "sparse_canonicalize_static_ws", "sparse_profile_enable",
-            "sparse_profile_reset", "sparse_profile_read", "sparse_read_rows")
+            "sparse_profile_reset", "sparse_profile_read", "sparse_read_rows", "sparse_check_finite")
 STATIC_WS_BYTES = 16 * 1024 * 1024  # SPARSE_STATIC_WS_BYTES
 
 
@@ -255,6 +257,11 @@ def sparse_sgd_table_step(p, buf, r, c, grad: Grad, cfg: SgdConfig, ws, d_err, s
     return LIB.sparse_sgd_table_step(_ptr(p, torch.float32, "p"), _ptr(buf, torch.float32, "buf"), int(r),
                                      int(c), ctypes.byref(grad), cfg, wp, wb, _ptr(d_err, torch.int32, "d_err"),
                                      _stream(stream))
+
+
+def sparse_check_finite(vals, n, d_err, stream=None) -> int:
+    return LIB.sparse_check_finite(_ptr(vals, torch.float32, "vals"), int(n), _ptr(d_err, torch.int32, "d_err"),
+                                   _stream(stream))
 
 
 def sparse_read_rows(table, r, c, idx, n, out, d_err, stream=None) -> int:

@@ -126,6 +126,7 @@ const char* sparse_status_string(sparse_status_t status)
     case SPARSE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case SPARSE_ERR_CUDA: return "CUDA error";
     case SPARSE_ERR_INTERNAL: return "internal: a bounded device wait gave up";
+    case SPARSE_ERR_NON_FINITE: return "a gradient value is NaN or infinite";
     }
     return "unknown status";
 }
@@ -294,6 +295,12 @@ sparse_status_t sparse_sgd_step(float* p, float* buf, int64_t dim, const int64_t
     grad.vals = g;
     grad.is_canonical = is_canonical;
     return sparse_sgd_table_step(p, buf, dim, 1, &grad, cfg, ws, ws_bytes, d_err, stream);
+}
+
+sparse_status_t sparse_check_finite(const float* vals, int64_t n, int32_t* d_err, cudaStream_t stream)
+{
+    if (n < 0 || d_err == nullptr || (n > 0 && vals == nullptr)) return SPARSE_ERR_INVALID_ARG;
+    return from_cuda(check_finite(vals, n, d_err, stream));
 }
 
 sparse_status_t sparse_read_rows(const float* table, int64_t r, int64_t c, const int64_t* idx, int64_t n, float* out,

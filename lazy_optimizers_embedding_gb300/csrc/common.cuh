@@ -278,6 +278,7 @@ cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, in
                       cudaStream_t s);
 cudaError_t read_rows(const float* table, int64_t r, int64_t c, const int64_t* idx, int64_t n, float* out, int vec4,
                       int32_t* d_err, cudaStream_t s);
+cudaError_t check_finite(const float* vals, int64_t n, int32_t* d_err, cudaStream_t s);
 cudaError_t csr_adam(const int64_t* row_off, const int32_t* cols, const float* vals, int64_t r,
                      int64_t c, int64_t nnz, const AdamParams& P, int32_t* d_err, cudaStream_t s);
 cudaError_t csr_sgd(const int64_t* row_off, const int32_t* cols, const float* vals, int64_t r,

@@ -1,4 +1,8 @@
-// gather.cu -- row gather: out[i, :] = table[idx[i], :], the lookup that feeds the
+// gather.cu -- streaming passes over caller arrays outside the step proper: the
+// finiteness check of gradient values ("DiskSparseAdam (DSA)" README, "Validated
+// Inputs") and the row gather.
+//
+// Row gather: out[i, :] = table[idx[i], :], the lookup that feeds the
 // forward pass ("DiskSparseAdam (DSA)" README, API read_rows(indices): the rows
 // of the table at the given indices, indices validated).
 //
@@ -78,6 +82,38 @@ static cudaError_t launch_gather(const float* table, int64_t r, int64_t c, const
     const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(occ) * num_sms())));
     SO_PROFILE("read_rows", s);
     launch(k_read_rows<T, NV, V>, dim3(blocks), dim3(kBlock), s, table, r, c, idx, n, out, d_err);
+    return cudaGetLastError();
+}
+
+// Any NaN or infinity among n values sets SPARSE_ERR_NON_FINITE.  Grid-stride,
+// 128-bit loads over the 16-byte aligned body, scalar head and tail.
+__global__ void __launch_bounds__(kBlock) k_check_finite(const float* __restrict__ vals, int64_t n, int64_t head,
+                                                         int32_t* d_err)
+{
+    pdl_enter();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    bool bad = false;
+    for (int64_t i = tid; i < head && i < n; i += stride) bad |= !isfinite(vals[i]);
+    const int64_t nv = (n - head) / 4;
+    const float4* body = reinterpret_cast<const float4*>(vals + head);
+    for (int64_t i = tid; i < nv; i += stride) {
+        const float4 q = __ldcs(body + i);
+        bad |= !isfinite(q.x) || !isfinite(q.y) || !isfinite(q.z) || !isfinite(q.w);
+    }
+    for (int64_t i = head + nv * 4 + tid; i < n; i += stride) bad |= !isfinite(vals[i]);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) set_error(d_err, SPARSE_ERR_NON_FINITE);
+}
+
+cudaError_t check_finite(const float* vals, int64_t n, int32_t* d_err, cudaStream_t s)
+{
+    if (n <= 0) return cudaSuccess;
+    const int64_t mis = static_cast<int64_t>((reinterpret_cast<uintptr_t>(vals) & 15u) / 4);
+    const int64_t head = mis ? std::min<int64_t>(4 - mis, n) : 0;
+    const int64_t want = (n / 4 + kBlock - 1) / kBlock + 1;
+    const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 8 * num_sms())));
+    SO_PROFILE("check_finite", s);
+    launch(k_check_finite, dim3(blocks), dim3(kBlock), s, vals, n, head, d_err);
     return cudaGetLastError();
 }
 

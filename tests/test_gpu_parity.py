@@ -665,3 +665,50 @@ def test_read_rows_bad_index_and_empty(cuda_lib):
     err2 = so.error_word()
     assert so.sparse_read_rows(dev(t), 10, 4, dev(idx), 0, out, err2) == so.OK
     assert so.sparse_read_rows(dev(t), 10, 0, dev(idx), 5, out, err2) == so.ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ non-finite gradient check
+@pytest.mark.parametrize("n,offset", [(1, 0), (7, 1), (1000, 0), (4099, 3), (262_147, 2)])
+def test_check_finite_matches_oracle(cuda_lib, n, offset):
+    """Values are read from an offset into a buffer, so the head / body / tail split is exercised."""
+    import torch
+    so = cuda_lib
+    rng = np.random.default_rng(n + offset)
+    base = rng.standard_normal(n + offset).astype(np.float32)
+    base[offset] = np.float32(3.0e38)
+    d = dev(base)
+    view = d[offset:]
+    for pos, bad in [(None, None), (0, np.nan), (n - 1, np.inf), (n // 2, -np.inf)]:
+        h = base[offset:].copy()
+        if pos is not None:
+            h[pos] = bad
+        view.copy_(torch.from_numpy(h))
+        err = so.error_word()
+        so.check(so.sparse_check_finite(view, n, err), "check_finite")
+        torch.cuda.synchronize()
+        assert int(err.item()) == oracle.check_finite(h)
+
+
+def test_check_finite_then_step_writes_nothing(cuda_lib):
+    """A non-finite value found before the step leaves every state array untouched (sticky error word)."""
+    import torch
+    so = cuda_lib
+    rng = np.random.default_rng(77)
+    R, c, n = 500, 32, 2000
+    p0 = rng.standard_normal((R, c)).astype(np.float32)
+    rows = rng.integers(0, R, n)
+    vals = rng.standard_normal((n, c)).astype(np.float32)
+    vals[1234, 5] = np.nan
+    p, m, v = dev(p0), torch.zeros((R, c), device="cuda"), torch.zeros((R, c), device="cuda")
+    ls = torch.zeros(R, dtype=torch.int64, device="cuda")
+    dvals = dev(vals)
+    err = so.error_word()
+    so.check(so.sparse_check_finite(dvals, n * c, err), "check_finite")
+    g = so.row_coo(dev(rows), dvals, False)
+    so.check(so.sparse_adam_table_step(p, m, v, ls, so.LAST_STEP_PER_ROW, R, c, g, 1,
+                                       so.AdamConfig(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8), so.DORMANCY_DECAY,
+                                       so.workspace(n, c, R), err), "step")
+    torch.cuda.synchronize()
+    assert int(err.item()) == so.ERR_NON_FINITE
+    assert host(p).tobytes() == p0.tobytes()
+    assert not host(m).any() and not host(v).any() and not host(ls).any()
