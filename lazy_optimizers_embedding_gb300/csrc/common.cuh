@@ -46,7 +46,10 @@ inline cudaError_t launch(void (*kernel)(P...), dim3 grid, dim3 block, cudaStrea
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kBlock = 256;            // threads per block of every kernel here
-constexpr int kPieceLen = 32;          // L: sorted entries summed by one team before a partial
+#ifndef SO_PIECE_LEN
+#define SO_PIECE_LEN 32
+#endif
+constexpr int kPieceLen = SO_PIECE_LEN;   // L: sorted entries summed by one team before a partial
 #ifndef SO_SORT_ITEMS
 #define SO_SORT_ITEMS 8
 #endif
