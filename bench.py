@@ -599,7 +599,8 @@ def run_workload(args):
                "sample": f"first {done} steps of the same workload; {spent:.1f} s of single-threaded oracle time"}
     line = {"metric": METRIC, "value": u_tot / el, "unit": "coords/s", "n_gpus": 1, "steps": K, "warmup": W,
             "ms_per_step": el / K * 1e3, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "mode": mode or "sgd", "rows": w.rows, "cols": c,
+            "config": {"workload": w.name.replace("_coo", "_read_rows") if mode == "gather" else w.name,
+                       "mode": mode or "sgd", "rows": w.rows, "cols": c,
                        "lookups_per_step": w.lookups, "distinct_batches": nb},
             "achieved_hbm_gbs": by_tot / el / 1e9, "hbm_frac_of_peak": by_tot / el / 1e9 / peak,
             "algorithmic_bytes_per_step": by_tot / K, "updated_coords_per_step": u_tot / K,
