@@ -188,8 +188,8 @@ struct WsLayout {
 };
 
 // counts[] word indices
-enum { kCtrPass0 = 1, kCtrRun = 5, kCntU = 8, kCntP = 9, kCntM = 10, kCntS = 11, kCntG = 12, kTicketM = 13,
-       kTicketS = 14, kCountsWords = 16 };
+enum { kCtrPass0 = 1, kCtrRun = 5, kCntU = 8, kCntP = 9, kCntM = 10, kCntS = 11, kCntG = 12, kTicketS = 14,
+       kCountsWords = 16 };
 
 WsLayout ws_layout(int64_t n, int64_t c, int64_t bound);
 

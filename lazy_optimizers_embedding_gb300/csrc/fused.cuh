@@ -629,14 +629,15 @@ __device__ __forceinline__ void store_partial(const Src& src, const float* __res
 }
 
 // Every piece of the input.  On a raw input the pieces range from one to
-// 2*kPieceLen-1 gradient rows, so they are handed out by atomic tickets, long
-// pieces first (the list run detection built: pieces of split segments, whose
-// partials the combine kernel waits for, and whole segments of more than
-// kShortLen entries), one per ticket, then short pieces kTicket per ticket
-// (their records one per lane).  A team requests its next ticket and that
-// ticket's records while it works on the current ones.  A canonical input (one
-// row per piece) is split statically, each team fetching the record of its
-// next piece during the current one.
+// 2*kPieceLen-1 gradient rows.  Long pieces come first (the list run detection
+// built: pieces of split segments, whose partials the combine kernel waits
+// for, and whole segments of more than kShortLen entries), split statically
+// over the teams; then short pieces are handed out by atomic tickets, kTicket
+// per ticket (their records one per lane), so that teams with less long work
+// take more of them.  A team requests its next piece's record, or its next
+// ticket and that ticket's records, while it works on the current ones.  A
+// canonical input (one row per piece) is split statically, each team fetching
+// the record of its next piece during the current one.
 template <int T, int NV, int V, class Src, class Epi>
 __global__ void __launch_bounds__(kBlock, kFusedMinBlocks) k_fused_rows(Src src, const float* __restrict__ vals,
                                                                         int64_t c, Epi epi, float* __restrict__ part,
@@ -660,14 +661,16 @@ __global__ void __launch_bounds__(kBlock, kFusedMinBlocks) k_fused_rows(Src src,
             const auto record = [&](uint32_t t, PieceInfo& r) {
                 if (tl == 0 && t < M) r = src.piece(src.multi_index(t));
             };
-            uint32_t ta = __shfl_sync(tmask, take(kTicketM), 0, T);
-            uint32_t tb = take(kTicketM);
+            // team g takes long pieces g, g + teams, ...: there are about two per
+            // team, and a static split spares every team the ticket round trip
+            // on one counter that all of them hit at the kernel's start
+            const uint32_t nteams = gridDim.x * kTeams;
+            uint32_t ta = blockIdx.x * kTeams + threadIdx.x / T;
+            uint32_t tb = ta + nteams;
             PieceInfo ra{}, rb{};
             record(ta, ra);
-            tb = __shfl_sync(tmask, tb, 0, T);
             while (ta < M) {
                 record(tb, rb);
-                const uint32_t tc = (tb < M) ? take(kTicketM) : tb;
                 const PieceInfo pc = shfl_piece<T>(ra, 0, tmask);
                 if (pc.multi())
                     store_partial<T, NV, V>(src, vals, c, part, nb, pc, tl, tmask);
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(kBlock, kFusedMinBlocks) k_fused_rows(Src src,
                     apply_single<T, NV, V, kLongIlp>(src, vals, c, epi, pc, tl, tmask);
                 ta = tb;
                 ra = rb;
-                tb = __shfl_sync(tmask, tc, 0, T);
+                tb += nteams;
             }
         }
         {   // short pieces
