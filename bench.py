@@ -426,6 +426,8 @@ def run_workload(args):
     from lazy_optimizers_embedding_gb300 import binding as so
     import oracle
     w, mode = WORKLOADS[args.workload]
+    if args.rows is not None and args.rows != w.rows:   # a smaller table, for ncu captures only
+        w = w.scaled(name=f"{w.name}_rows{args.rows}", rows=args.rows)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     K, W = args.steps, args.warmup
@@ -659,9 +661,9 @@ def main(argv=None):
     ap.add_argument("--workload", choices=["zipf10m"] + sorted(WORKLOADS), default="zipf10m",
                     help="another specified workload instead of the headline one (1 GPU, one JSON line)")
     ap.add_argument("--rows", type=int, default=None,
-                    help="table rows (default 10,000,000); smaller tables are for ncu captures, not bench lines")
+                    help="table rows (default: the workload's); smaller tables are for ncu captures, not bench lines")
     args = ap.parse_args(argv)
-    if args.rows is not None and args.rows != W_CFG.rows:
+    if args.rows is not None and args.rows != W_CFG.rows and args.workload == "zipf10m":
         globals()["W_CFG"] = W_CFG.scaled(name=f"{W_CFG.name}_rows{args.rows}", rows=args.rows)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
