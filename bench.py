@@ -309,6 +309,32 @@ def run_ours(args):
     our_kernels = sum(l for l, _ in prof.values())
     check_err()
 
+    # ---- per-step distribution of the same steps (events around every step), and the same
+    # steps again with L2 flushed before each (a buffer of twice the L2 size written first)
+    def timed_steps(before=None):
+        evs = []
+        for b in timed:
+            if before is not None:
+                before()
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step(b)
+            z.record(stream)
+            evs.append((a, z))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(z) for a, z in evs]
+
+    per_step = timed_steps()
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or 129 * 2 ** 20)
+    flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=device)
+    cold = timed_steps(lambda: flush.fill_(float(len(flush) % 7)))
+    del flush
+    check_err()
+
+    def pct(xs):
+        return {"median": float(np.median(xs)), "p10": float(np.percentile(xs, 10)),
+                "p90": float(np.percentile(xs, 90))}
+
     # ---- end to end: each step's inputs copied from pinned host memory (copy stream,
     # double-buffered), the C-ABI step, the error word read back to pinned host memory
     h_in = [(torch.from_numpy(i).pin_memory(), torch.from_numpy(x).pin_memory()) for i, x in batches]
@@ -359,7 +385,7 @@ def run_ours(args):
         hm, hv = np.zeros_like(hp), np.zeros_like(hp)
         hls = np.zeros(w.rows, np.int64)
         units, spent, done = oracle_steps(hp, hm, hv, hls, batches, u_rows, 1, K + W, dd, args.cpu_seconds)
-        cpu = {"value": units / spent, "unit": "coords/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": units / spent, "unit": "coords/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
                "sample": f"first {done} steps of the same workload (full-size table, same seeded inputs); "
                          f"{spent:.1f} s of single-threaded oracle time (canonicalise + update in fp64)"}
 
@@ -393,6 +419,11 @@ def run_ours(args):
                          "avg_launch_us": dom_avg_s * 1e6},
             "kernel_share": {k: {"launches": l, "ms": ms, "share": ms / total_prof if total_prof else None}
                              for k, (l, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1])},
+            "per_step_ms": dict(pct(per_step), steps=len(per_step),
+                                method="CUDA events around each of the K steps, a pass after the timed one; the "
+                                       "event between two steps also costs their overlap"),
+            "cold_l2_ms": dict(pct(cold), flush_bytes=2 * l2_bytes,
+                               method="the same steps, each after writing a buffer of twice the L2 size"),
             "clocks": dict(clocks or {}, window="timed region plus 1 s of the same step loop"),
             "e2e": {"value": e2e_units / e2e_elapsed, "unit": "coords/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo},
@@ -597,7 +628,7 @@ def run_workload(args):
             done += 1
             if spent >= args.cpu_seconds:
                 break
-        cpu = {"value": cu / spent, "unit": "coords/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": cu / spent, "unit": "coords/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
                "sample": f"first {done} steps of the same workload; {spent:.1f} s of single-threaded oracle time"}
     line = {"metric": METRIC, "value": u_tot / el, "unit": "coords/s", "n_gpus": 1, "steps": K, "warmup": W,
             "ms_per_step": el / K * 1e3, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
@@ -642,7 +673,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy PCG64: Zipf row indices, normal values; random-init table)",
             "config": dict(config_dict(dd, n_batches, 1), parallelism="host CPU oracle, 1 thread"),
-            "cpu_baseline": {"value": val, "unit": "coords/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": val, "unit": "coords/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"{K} timed steps after {W} warm-up steps of the full workload"},
             "e2e": {"value": val, "unit": "coords/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
