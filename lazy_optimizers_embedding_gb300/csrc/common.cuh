@@ -43,6 +43,24 @@ inline cudaError_t launch(void (*kernel)(P...), dim3 grid, dim3 block, cudaStrea
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
 }
 
+// The same with dynamic shared memory.
+template <class... P, class... A>
+inline cudaError_t launch_smem(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               A&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kBlock = 256;            // threads per block of every kernel here

@@ -31,11 +31,12 @@
 
 namespace so {
 
-// Blocks of kBlock threads per SM the row kernel is compiled for (3: at most 80
-// registers, 24 warps per SM), short pieces per work ticket (kTicket), gradient
-// rows a lane requests at once (kRowIlp), threads of a combine block and the
-// partial pairs a lane of it requests at once (kCombineIlp).  Overridable at
-// build time for tuning sweeps.
+// Blocks of kRowBlock threads per SM the row kernel is compiled for (3 of 256:
+// at most 80 registers, 24 warps per SM), short pieces per work ticket
+// (kTicket), gradient rows a lane requests at once (kRowIlp, kLongIlp), rows of
+// a long piece staged in shared memory per round (kLongStage), threads of a
+// combine block and the partial pairs a lane of it requests at once
+// (kCombineIlp).  Overridable at build time for tuning sweeps.
 #ifndef SO_FUSED_MIN_BLOCKS
 #define SO_FUSED_MIN_BLOCKS 3
 #endif
@@ -51,10 +52,20 @@ namespace so {
 #ifndef SO_COMBINE_ILP
 #define SO_COMBINE_ILP 8
 #endif
+#ifndef SO_ROW_BLOCK
+#define SO_ROW_BLOCK 256
+#endif
+constexpr int kRowBlock = SO_ROW_BLOCK;   // threads of a row-kernel block
+#ifndef SO_LONG_STAGE
+#define SO_LONG_STAGE 8
+#endif
+// Gradient rows of a long piece a team stages in shared memory per round (0:
+// the rows are requested into registers, kLongIlp at a time).
+constexpr int kLongStage = SO_LONG_STAGE;
 constexpr int kFusedMinBlocks = SO_FUSED_MIN_BLOCKS;
 constexpr int kTicket = SO_TICKET;
 constexpr int kRowIlp = SO_ROW_ILP;
-constexpr int kLongIlp = SO_LONG_ILP;   // gradient rows requested at once in a long piece
+constexpr int kLongIlp = SO_LONG_ILP;   // gradient rows requested at once in a long piece (unstaged shapes)
 constexpr int kCombineBlock = 128;
 constexpr int kCombineIlp = SO_COMBINE_ILP;
 
@@ -484,6 +495,65 @@ __device__ __forceinline__ void sum_rest(const Src& src, const PiecePerms<T>& pp
     }
 }
 
+// ------------------------------------------------------------ staged long pieces
+// With kLongStage > 0 a long piece's gradient rows travel through the team's
+// shared buffer instead of registers: every lane copies its 16 bytes of each of
+// up to kLongStage rows with cp.async, waits for its own copies and adds its
+// slice of the rows in entry order with TwoSum compensation, the same
+// operations in the same order as sum_rest.  A lane reads back only what it
+// copied itself, so no barrier is needed.  For rows of whole 16-byte vectors in
+// one chunk (the float4 instantiations) and teams of 8 lanes or more.
+template <int T, int NV, int V, class Src>
+__host__ __device__ constexpr bool long_staged()
+{
+    return kLongStage > 0 && Src::kTickets && NV == 1 && V == 4 && T >= 8;
+}
+// dynamic shared memory of a row-kernel block: every team kLongStage rows of at most 4T floats
+__host__ __device__ constexpr size_t long_stage_bytes() { return static_cast<size_t>(kRowBlock) * kLongStage * 16; }
+
+template <int T>
+__device__ __forceinline__ void staged_rest(const PiecePerms<T>& pp, const PieceInfo& pc, const float* __restrict__ vals,
+                                            int64_t c, int tl, unsigned tmask, uint32_t buf_s, float (&s)[4],
+                                            float (&cm)[4])
+{
+    const int rest = static_cast<int>(pc.end - pc.start) - 1;
+    const uint32_t row_bytes = static_cast<uint32_t>(c) * 4u;
+    const bool mine = tl * 4 < c;
+    const uint32_t lane_s = buf_s + static_cast<uint32_t>(tl) * 16u;
+    const float* lane_v = vals + tl * 4;
+    for (int k0 = 0; k0 < rest; k0 += kLongStage) {
+        const int cnt = (rest - k0) < kLongStage ? (rest - k0) : kLongStage;
+#pragma unroll
+        for (int q = 0; q < PiecePerms<T>::kPerLane; ++q) {
+            // rows k0 .. k0+cnt-1 whose input positions sit in slot q of lanes 0..T-1
+            const int lo = q * T > k0 ? q * T : k0;
+            const int hi = (q + 1) * T < k0 + cnt ? (q + 1) * T : k0 + cnt;
+            for (int i = lo; i < hi; ++i) {
+                const uint32_t pr = __shfl_sync(tmask, pp.pm[q], i - q * T, T);
+                if (mine)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                     lane_s + static_cast<uint32_t>(i - k0) * row_bytes),
+                                 "l"(lane_v + static_cast<int64_t>(pr) * c)
+                                 : "memory");
+            }
+        }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        if (mine) {
+            for (int r = 0; r < cnt; ++r) {
+                float4 x;
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                             : "r"(lane_s + static_cast<uint32_t>(r) * row_bytes)
+                             : "memory");
+                two_sum_acc(s[0], cm[0], x.x);
+                two_sum_acc(s[1], cm[1], x.y);
+                two_sum_acc(s[2], cm[2], x.z);
+                two_sum_acc(s[3], cm[3], x.w);
+            }
+        }
+    }
+}
+
 // Pieces of a split segment [s0, s1) and their partial-sum slots.  The first
 // piece starts at s0; piece i >= 1 starts at q1 + (i-1)*kPieceLen, where q1 is
 // the smallest multiple of kPieceLen >= s0 + kPieceLen (see run detection).  A
@@ -628,24 +698,72 @@ __device__ __forceinline__ void store_partial(const Src& src, const float* __res
     }
 }
 
+// store_partial and apply_single for a long piece through the team's stage.
+template <int T, class Src>
+__device__ __forceinline__ void store_partial_staged(const Src& src, const float* __restrict__ vals, int64_t c,
+                                                     float* __restrict__ part, int64_t nb, const PieceInfo& pc,
+                                                     int tl, unsigned tmask, uint32_t buf_s)
+{
+    float* ps = part + part_slot(pc.start, nb) * 2 * c;
+    PiecePerms<T> pp;
+    pp.load(src, pc, tl);
+    float s[1][4], cm[1][4];
+    first_row<T, 1, 4>(vals, c, 0, tl, pc.perm0, s);
+    zero_comp<1, 4>(cm);
+    staged_rest<T>(pp, pc, vals, c, tl, tmask, buf_s, s[0], cm[0]);
+    const int64_t col = static_cast<int64_t>(tl) * 4;
+    if (col < c) {
+        st_part<4>(ps + col, s[0]);
+        st_part<4>(ps + c + col, cm[0]);
+    }
+}
+
+template <int T, class Src, class Epi>
+__device__ __forceinline__ void apply_single_staged(const Src& src, const float* __restrict__ vals, int64_t c,
+                                                    const Epi& epi, const PieceInfo& pc, int tl, unsigned tmask,
+                                                    uint32_t buf_s)
+{
+    const int64_t* lp = epi.stage_last(pc);
+    PiecePerms<T> pp;
+    if (pc.end - pc.start > 1) pp.load(src, pc, tl);
+    float x[1][Epi::kArrays][4];
+    load_state<T, 1, 4>(epi, pc, c, 0, tl, x);
+    const int64_t last = lp ? *lp : 0;
+    float s[1][4];
+    first_row<T, 1, 4>(vals, c, 0, tl, pc.perm0, s);
+    if (pc.end - pc.start > 1) {
+        float cm[1][4];
+        zero_comp<1, 4>(cm);
+        staged_rest<T>(pp, pc, vals, c, tl, tmask, buf_s, s[0], cm[0]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[0][i] = __fadd_rn(s[0][i], cm[0][i]);
+    }
+    const typename Epi::Row row = epi.make_row(pc, last);
+    const int64_t col = static_cast<int64_t>(tl) * 4;
+    if (col < c) epi.template apply<4>(row, col, x[0], s[0]);
+    epi.end_row(row, tl, tmask);
+}
+
 // Every piece of the input.  On a raw input the pieces range from one to
 // 2*kPieceLen-1 gradient rows.  Long pieces come first (the list run detection
 // built: pieces of split segments, whose partials the combine kernel waits
 // for, and whole segments of more than kShortLen entries), split statically
-// over the teams; then short pieces are handed out by atomic tickets, kTicket
+// over the teams, their gradient rows staged through shared memory
+// (kLongStage rows a round, where the shape allows), so that the registers go
+// to the short pieces' loads; then short pieces are handed out by atomic tickets, kTicket
 // per ticket (their records one per lane), so that teams with less long work
 // take more of them.  A team requests its next piece's record, or its next
 // ticket and that ticket's records, while it works on the current ones.  A
 // canonical input (one row per piece) is split statically, each team fetching
 // the record of its next piece during the current one.
 template <int T, int NV, int V, class Src, class Epi>
-__global__ void __launch_bounds__(kBlock, kFusedMinBlocks) k_fused_rows(Src src, const float* __restrict__ vals,
+__global__ void __launch_bounds__(kRowBlock, kFusedMinBlocks) k_fused_rows(Src src, const float* __restrict__ vals,
                                                                         int64_t c, Epi epi, float* __restrict__ part,
                                                                         int64_t nb, int32_t* d_err)
 {
     pdl_enter();
     if (read_error(d_err)) return;
-    constexpr int kTeams = kBlock / T;
+    constexpr int kTeams = kRowBlock / T;
     const int lane = threadIdx.x & 31;
     const int tl = lane & (T - 1);
     const unsigned tmask = (T == 32) ? kFull : (((1u << T) - 1u) << (lane & ~(T - 1)));
@@ -669,13 +787,25 @@ __global__ void __launch_bounds__(kBlock, kFusedMinBlocks) k_fused_rows(Src src,
             uint32_t tb = ta + nteams;
             PieceInfo ra{}, rb{};
             record(ta, ra);
+            [[maybe_unused]] uint32_t buf_s = 0;
+            if constexpr (long_staged<T, NV, V, Src>()) {
+                extern __shared__ float4 so_long_stage[];
+                buf_s = static_cast<uint32_t>(__cvta_generic_to_shared(so_long_stage)) +
+                        static_cast<uint32_t>((threadIdx.x / T) * kLongStage) * static_cast<uint32_t>(c) * 4u;
+            }
             while (ta < M) {
                 record(tb, rb);
                 const PieceInfo pc = shfl_piece<T>(ra, 0, tmask);
-                if (pc.multi())
+                if constexpr (long_staged<T, NV, V, Src>()) {
+                    if (pc.multi())
+                        store_partial_staged<T>(src, vals, c, part, nb, pc, tl, tmask, buf_s);
+                    else
+                        apply_single_staged<T>(src, vals, c, epi, pc, tl, tmask, buf_s);
+                } else if (pc.multi()) {
                     store_partial<T, NV, V>(src, vals, c, part, nb, pc, tl, tmask);
-                else
+                } else {
                     apply_single<T, NV, V, kLongIlp>(src, vals, c, epi, pc, tl, tmask);
+                }
                 ta = tb;
                 ra = rb;
                 tb += nteams;
@@ -850,10 +980,10 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_split(Src src, int64_
 
 // ------------------------------------------------------------ launch
 template <class K>
-int max_blocks(K kernel, int threads)
+int max_blocks(K kernel, int threads, size_t smem = 0)
 {
     int occ = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem);
     return occ > 0 ? occ : 1;
 }
 
@@ -863,13 +993,26 @@ template <int T, int NV, int V, class Src, class Epi>
 cudaError_t launch_shape(const Src& src, int64_t max_pieces, int64_t max_split, const float* vals, int64_t c,
                          const Epi& epi, float* part, int64_t nb, int32_t* d_err, cudaStream_t s)
 {
-    constexpr int kTeams = kBlock / T;
+    constexpr int kTeams = kRowBlock / T;
     {
-        static const int occ = max_blocks(k_fused_rows<T, NV, V, Src, Epi>, kBlock);
+        constexpr size_t smem = long_staged<T, NV, V, Src>() ? long_stage_bytes() : 0;
+        static const int occ = [] {
+            if (smem > 0) {
+                // room for kFusedMinBlocks blocks (plus 1 KB reserved each) of the 228 KB per SM
+                const int pct = static_cast<int>(std::min<size_t>(
+                    100, (kFusedMinBlocks * (smem + 1024) * 100 + 228 * 1024 - 1) / (228 * 1024)));
+                cudaFuncSetAttribute(k_fused_rows<T, NV, V, Src, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem));
+                cudaFuncSetAttribute(k_fused_rows<T, NV, V, Src, Epi>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     pct);
+            }
+            return max_blocks(k_fused_rows<T, NV, V, Src, Epi>, kRowBlock, smem);
+        }();
         const int64_t cap = static_cast<int64_t>(occ) * num_sms();
         const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cap, (max_pieces + kTeams - 1) / kTeams)));
         SO_PROFILE(Epi::kName, s);
-        launch(k_fused_rows<T, NV, V, Src, Epi>, dim3(blocks), dim3(kBlock), s, src, vals, c, epi, part, nb, d_err);
+        launch_smem(k_fused_rows<T, NV, V, Src, Epi>, dim3(blocks), dim3(kRowBlock), smem, s, src, vals, c, epi, part,
+                    nb, d_err);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
