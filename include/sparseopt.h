@@ -59,7 +59,8 @@
  *             coordinate is touched when it is present in the canonical sparse
  *             structure, whatever its value; nothing else is read or written.
  *   Limits.   Raw (non-canonical) input: n <= 2^30 entries, keys < 2^32.
- *             Canonical row-COO input: n < 2^31 rows.
+ *             Canonical row-COO input: n < 2^31 rows, tables of at most 2^32
+ *             rows (1-D: dim <= 2^32).  CSR input: no limit beyond int64.
  */
 #ifndef SPARSEOPT_H
 #define SPARSEOPT_H

@@ -13,7 +13,7 @@ using namespace so;
 
 constexpr int64_t kMaxRawN = int64_t(1) << 30;
 constexpr int64_t kMaxCanonN = (int64_t(1) << 31) - 1;   // canonical row-COO rows (32-bit positions)
-constexpr int64_t kMaxRawBound = int64_t(1) << 32;
+constexpr int64_t kMaxRawBound = int64_t(1) << 32;   // raw keys, and rows of a canonical row-COO table
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -93,7 +93,7 @@ sparse_status_t check_grad(const sparse_grad_t* g, int64_t r, int64_t c)
     if (g->form == SPARSE_GRAD_ROW_COO) {
         if (g->n > 0 && (g->row_idx == nullptr || g->vals == nullptr)) return SPARSE_ERR_INVALID_ARG;
         if (!g->is_canonical && (g->n > kMaxRawN || r > kMaxRawBound)) return SPARSE_ERR_INVALID_ARG;
-        if (g->is_canonical && g->n > kMaxCanonN) return SPARSE_ERR_INVALID_ARG;
+        if (g->is_canonical && (g->n > kMaxCanonN || r > kMaxRawBound)) return SPARSE_ERR_INVALID_ARG;
         return SPARSE_OK;
     }
     if (g->form == SPARSE_GRAD_CSR) {

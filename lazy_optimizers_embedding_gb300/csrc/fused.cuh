@@ -71,7 +71,7 @@ constexpr int kCombineIlp = SO_COMBINE_ILP;
 
 struct PieceInfo {
     uint32_t start, end;  // sorted positions [start, end)
-    int64_t key;          // table row
+    uint32_t key;         // table row (< 2^32: raw keys and canonical rows both are)
     uint32_t uf;          // segment index (row of a canonical output) | flags
     uint32_t perm0;       // input position of the first entry
     // kMultiFlag: segment spans several pieces; kLongFlag: one long piece
@@ -140,7 +140,7 @@ struct CanonSrc {
         PieceInfo p;
         p.start = static_cast<uint32_t>(j);
         p.end = static_cast<uint32_t>(j + 1);
-        p.key = rows[j];
+        p.key = static_cast<uint32_t>(rows[j]);
         p.uf = static_cast<uint32_t>(j) & kSingleMask;
         p.perm0 = static_cast<uint32_t>(j);
         return p;
@@ -663,7 +663,7 @@ __device__ __forceinline__ PieceInfo shfl_piece(const PieceInfo& p, int from, un
     PieceInfo q;
     q.start = __shfl_sync(tmask, p.start, from, T);
     q.end = __shfl_sync(tmask, p.end, from, T);
-    q.key = __shfl_sync(tmask, static_cast<long long>(p.key), from, T);
+    q.key = __shfl_sync(tmask, p.key, from, T);
     q.uf = __shfl_sync(tmask, p.uf, from, T);
     q.perm0 = __shfl_sync(tmask, p.perm0, from, T);
     return q;

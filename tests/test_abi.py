@@ -54,3 +54,18 @@ def test_host_side_queries(lib_path):
     # workspace grows about linearly in n (keys, positions, pieces, partial slots)
     assert big < 262_144 * (4 * 4 + 16 + 4 + 2 * 2 * 128 * 4 / 32 * 2 + 64)
     assert so.sparse_workspace_size(-1, 1, 1) == 0
+
+
+def test_row_count_limits_rejected_on_the_host(lib_path):
+    """Row-COO tables of more than 2^32 rows are refused before anything is enqueued (raw keys
+    and the rows of a canonical table are 32-bit inside the library); the pointers are never
+    dereferenced, so placeholders serve."""
+    import ctypes
+    from lazy_optimizers_embedding_gb300 import binding as so
+    fake = ctypes.c_void_p(256)
+    cfg = so.AdamConfig(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8)
+    for canonical in (0, 1):
+        g = so.Grad(form=so.GRAD_ROW_COO, n=4, row_idx=256, vals=256, is_canonical=canonical)
+        rc = so.LIB.sparse_adam_table_step(fake, fake, fake, fake, so.LAST_STEP_PER_ROW, (1 << 32) + 1, 1,
+                                           ctypes.byref(g), 1, cfg, so.DORMANCY_DECAY, fake, 1 << 20, fake, None)
+        assert rc == so.ERR_INVALID_ARG
