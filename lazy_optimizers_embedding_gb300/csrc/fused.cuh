@@ -44,7 +44,7 @@ namespace so {
 #define SO_TICKET 4
 #endif
 #ifndef SO_ROW_ILP
-#define SO_ROW_ILP 4
+#define SO_ROW_ILP 3
 #endif
 #ifndef SO_LONG_ILP
 #define SO_LONG_ILP 4
