@@ -97,8 +97,8 @@ constexpr int kRadixLook = SO_RADIX_LOOK;          // predecessor tiles a radix 
 constexpr uint32_t kSingleMask = 0x3fffffffu;   // segment index bits of a piece record
 constexpr uint32_t kMultiFlag = 0x80000000u;    // piece of a segment split into several pieces
 constexpr uint32_t kLongFlag = 0x40000000u;     // whole segment of more than kShortLen entries
-// Pieces of at most kShortLen entries go to the short-piece kernel; longer ones
-// (and all pieces of split segments) to the long-piece kernel.
+// Pieces of at most kShortLen entries are the row kernel's short pieces; longer
+// ones (and all pieces of split segments) its long pieces, worked first.
 #ifndef SO_SHORT_LEN
 #define SO_SHORT_LEN 4
 #endif
@@ -223,7 +223,7 @@ struct SortWs {
     float* part;          // partial sums: [2*nb slots][2][c]
     uint32_t* bh;         // [hist_blocks][4][256] digit histograms, one set per block
     uint32_t* gh;         // [4][256] whole-input digit histograms of the later passes
-    uint32_t* counts;     // [16]: tile counters, U, P, M, S, G, work tickets
+    uint32_t* counts;     // [16]: tile counters, U, P, M, S, G, the short pieces' ticket counter
     uint32_t* rstatus;    // [passes][sort_tiles][256]
     unsigned long long* dstatus;  // [run_tiles]
     uint32_t* scnt;       // [2*nb] groups merged per split segment (zeroed with the control block)
