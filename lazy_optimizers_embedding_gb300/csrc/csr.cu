@@ -362,11 +362,17 @@ struct CsrSgdOp {
     __device__ __forceinline__ SgdEpi::Row make_row(int64_t row, int64_t) const { return SgdEpi::Row{row}; }
 };
 
+#ifndef SO_CSR_BLOCKS_PER_SM
+#define SO_CSR_BLOCKS_PER_SM 16
+#endif
+// Blocks of the CSR kernels: one warp per group of 32 rows, at most
+// SO_CSR_BLOCKS_PER_SM blocks per SM (several waves: a block that finds only
+// empty groups retires quickly and its slot takes the next block).
 static int group_blocks(int64_t r)
 {
     const int64_t groups = (r + 31) / 32;
     const int64_t want = (groups + kBlock / 32 - 1) / (kBlock / 32);
-    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 16 * num_sms())));
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(SO_CSR_BLOCKS_PER_SM) * num_sms())));
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
