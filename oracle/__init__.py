@@ -7,7 +7,8 @@ arithmetic, scalar loops, a library sort) plus the tiny dense emulator in
 (``lazy_optimizers_embedding_gb300``) never does, and the two share no code.
 
 Status codes: 0 ok, 1 invalid argument, 2 index out of range, 3 not canonical,
-4 step order (t <= last_step), 8 out of host memory.
+4 step order (t <= last_step), 8 non-finite gradient value, 9 corrupted moment
+state (NaN / infinite m or v, negative v), 100 out of host memory.
 """
 from __future__ import annotations
 
@@ -33,6 +34,7 @@ FORM_CSR = 1
 
 OK, ERR_INVALID_ARG, ERR_INDEX_OUT_OF_RANGE, ERR_NOT_CANONICAL, ERR_STEP_ORDER = 0, 1, 2, 3, 4
 ERR_NON_FINITE = 8
+ERR_BAD_STATE = 9
 
 
 def build(force: bool = False) -> str:
@@ -69,6 +71,8 @@ def lib():
         l.oracle_read_rows.argtypes = [_P, _I64, _I64, _P, _I64, _P]
         l.oracle_check_finite.argtypes = [_P, _I64]
         l.oracle_check_finite.restype = _INT
+        l.oracle_check_state.argtypes = [_P, _P, _I64, _I64, _INT, _P, _I64, _P, _P]
+        l.oracle_check_state.restype = _INT
         l.oracle_read_rows.restype = _INT
         l.oracle_sgd_table_step.argtypes = [_P, _P, _INT, _I64, _I64, _INT,
                                             _P, _I64, _INT, _P, _P, _P, _D, _D, _D]
@@ -194,6 +198,24 @@ def check_finite(vals) -> int:
     """ERR_NON_FINITE when any value is NaN or infinite, else OK."""
     vals = _c(vals, np.float32)
     return lib().oracle_check_finite(_ptr(vals), vals.size)
+
+
+def check_state(m, v, *, rows=None, row_off=None, cols=None) -> int:
+    """Validation of the Adam moments a step would read ("DiskSparseAdam (DSA)" README,
+    "Validated Inputs": NaN / negative moment rows).  m, v: [r, c] (or [dim]) fp32;
+    the gradient's structure as row-COO rows (any order, repeats allowed) or CSR
+    (row_off, cols).  Returns ERR_BAD_STATE, ERR_INDEX_OUT_OF_RANGE, ERR_NOT_CANONICAL
+    (malformed CSR) or OK."""
+    m, v = _c(m, np.float32), _c(v, np.float32)
+    assert m.shape == v.shape
+    r = m.shape[0]
+    c = 1 if m.ndim == 1 else m.shape[1]
+    if row_off is not None:
+        row_off, cols = _c(row_off, np.int64), _c(cols, np.int32)
+        return lib().oracle_check_state(_ptr(m), _ptr(v), r, c, FORM_CSR, None, cols.shape[0], _ptr(row_off),
+                                        _ptr(cols))
+    rows = _c(rows, np.int64)
+    return lib().oracle_check_state(_ptr(m), _ptr(v), r, c, FORM_ROW_COO, _ptr(rows), rows.shape[0], None, None)
 
 
 def read_rows(table, idx, *, check=True):

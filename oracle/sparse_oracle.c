@@ -27,12 +27,14 @@
  *        error.
  *   [S8] same README, API read_rows(indices): the rows of the table at the given
  *        indices (the lookup that feeds the forward pass), indices validated.
+ *   [S10] same README, "Validated Inputs": NaN or negative moment rows have an
+ *        explicit, defined behaviour (here: an explicit error before any write).
  *   [S7] same README, "Explicit Weight Decay Semantics" and the API's
  *        weight_decay / weight_decay_mode (Euclidean case, k = 0):
  *        "l2" adds wd*w to the gradient (classic Adam L2); "decoupled" adds
  *        wd*w to the descent direction (AdamW).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - duplicates are summed in fp64 in input order, starting from the first
  *     value, and rounded once to fp32 (a single value passes through unchanged);
  *   - a coordinate is touched when it is present in the canonical structure,
@@ -64,6 +66,7 @@ enum {
     OR_ERR_NOT_CANONICAL = 3,
     OR_ERR_STEP_ORDER = 4,
     OR_ERR_NON_FINITE = 8,
+    OR_ERR_BAD_STATE = 9,
     OR_ERR_NO_MEMORY = 100
 };
 
@@ -482,4 +485,47 @@ int oracle_check_finite(const float* vals, int64_t n)
     for (int64_t i = 0; i < n; ++i)
         if (!isfinite(vals[i])) return OR_ERR_NON_FINITE;
     return OR_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* moment-state validation [S10]                                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Checks the Adam moments a step with this gradient would read.  The touched
+ * coordinates are every column of each listed row (row-COO: row_idx[n], any
+ * order, repeats allowed) or the listed (row, cols[j]) pairs (CSR: row_off[r+1],
+ * cols[n], validated like a CSR gradient).  Returns
+ *   OR_ERR_INDEX_OUT_OF_RANGE  a listed row outside [0, r),
+ *   OR_ERR_BAD_STATE           a touched m that is NaN or infinite, or a touched
+ *                              v that is NaN, infinite or below zero (-0.0 is
+ *                              not below zero),
+ *   OR_OK                      otherwise.
+ * Untouched coordinates are never read.  Nothing is written.
+ */
+int oracle_check_state(const float* m, const float* v, int64_t r, int64_t c, int form,
+                       const int64_t* row_idx, int64_t n, const int64_t* row_off, const int32_t* cols)
+{
+    if (r < 0 || c < 1 || n < 0) return OR_ERR_INVALID_ARG;
+    if (form == OR_FORM_ROW_COO) {
+        for (int64_t i = 0; i < n; ++i)
+            if (row_idx[i] < 0 || row_idx[i] >= r) return OR_ERR_INDEX_OUT_OF_RANGE;
+        for (int64_t i = 0; i < n; ++i)
+            for (int64_t col = 0; col < c; ++col) {
+                const int64_t k = row_idx[i] * c + col;
+                if (!isfinite(m[k]) || !isfinite(v[k]) || v[k] < 0.0f) return OR_ERR_BAD_STATE;
+            }
+        return OR_OK;
+    }
+    if (form == OR_FORM_CSR) {
+        const int rc = oracle_csr_validate(row_off, cols, r, c, n, 0);
+        if (rc) return rc;
+        for (int64_t row = 0; row < r; ++row)
+            for (int64_t j = row_off[row]; j < row_off[row + 1]; ++j) {
+                const int64_t k = row * c + cols[j];
+                if (!isfinite(m[k]) || !isfinite(v[k]) || v[k] < 0.0f) return OR_ERR_BAD_STATE;
+            }
+        return OR_OK;
+    }
+    return OR_ERR_INVALID_ARG;
 }

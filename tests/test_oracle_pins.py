@@ -614,3 +614,71 @@ def test_p12_check_finite():
         h[99, 7] = bad
         assert oracle.check_finite(h) == oracle.ERR_NON_FINITE
         assert oracle.check_finite(h) == (oracle.ERR_NON_FINITE if not np.isfinite(h).all() else oracle.OK)
+
+
+# --------------------------------------------------------------------------
+# P13: corrupted moment state (DSA README, "Validated Inputs": NaN / negative
+# moment rows).  Pinned against numpy's isfinite and comparison on the gathered
+# coordinates, over random tables with planted specials (brute force).
+# --------------------------------------------------------------------------
+_SPECIALS = [np.nan, np.inf, -np.inf, -1e-3, -1e-42, -0.0, 1e-42, 0.0]
+
+
+def _numpy_state_ok(m, v, rows=None, row_off=None, cols=None):
+    if row_off is not None:
+        rr = np.repeat(np.arange(m.shape[0]), np.diff(row_off))
+        mt, vt = m[rr, cols], v[rr, cols]
+    else:
+        mt, vt = m[rows], v[rows]
+    return bool(np.isfinite(mt).all() and np.isfinite(vt).all() and (vt >= 0).all())
+
+
+def test_p13_check_state_matches_numpy_brute_force():
+    rng = np.random.default_rng(41)
+    seen = {oracle.OK: 0, oracle.ERR_BAD_STATE: 0}
+    for trial in range(400):
+        r, c = int(rng.integers(1, 9)), int(rng.integers(1, 5))
+        m = rng.standard_normal((r, c)).astype(np.float32)
+        v = np.abs(rng.standard_normal((r, c))).astype(np.float32)
+        for _ in range(int(rng.integers(0, 3))):
+            arr = m if rng.random() < 0.5 else v
+            arr[rng.integers(0, r), rng.integers(0, c)] = _SPECIALS[rng.integers(0, len(_SPECIALS))]
+        if trial % 2 == 0:
+            rows = rng.integers(0, r, int(rng.integers(0, 6)))
+            got = oracle.check_state(m, v, rows=rows)
+            ok = _numpy_state_ok(m, v, rows=rows)
+        else:
+            counts = rng.integers(0, c + 1, r)
+            row_off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+            cols = np.concatenate([np.sort(rng.choice(c, k, replace=False)) for k in counts]).astype(np.int32) \
+                if counts.sum() else np.zeros(0, np.int32)
+            got = oracle.check_state(m, v, row_off=row_off, cols=cols)
+            ok = _numpy_state_ok(m, v, row_off=row_off, cols=cols)
+        assert got == (oracle.OK if ok else oracle.ERR_BAD_STATE), (trial, got, ok)
+        seen[got] += 1
+    assert seen[oracle.OK] > 50 and seen[oracle.ERR_BAD_STATE] > 50
+
+
+def test_p13_check_state_cases():
+    m = np.zeros((4, 3), np.float32)
+    v = np.zeros((4, 3), np.float32)
+    v[1, 2] = np.float32(-0.0)                     # -0.0 is not below zero
+    m[2, 0] = np.float32(-1e-42)                   # a negative first moment is legal
+    assert oracle.check_state(m, v, rows=np.array([1, 2, 1])) == oracle.OK
+    v[3, 1] = np.float32(-1e-45)                   # the smallest negative v
+    assert oracle.check_state(m, v, rows=np.array([0, 1, 2])) == oracle.OK   # row 3 untouched
+    assert oracle.check_state(m, v, rows=np.array([3])) == oracle.ERR_BAD_STATE
+    # CSR: only the listed columns of a row are read
+    row_off = np.array([0, 0, 0, 0, 2], np.int64)
+    assert oracle.check_state(m, v, row_off=row_off, cols=np.array([0, 2], np.int32)) == oracle.OK
+    assert oracle.check_state(m, v, row_off=row_off, cols=np.array([1, 2], np.int32)) == oracle.ERR_BAD_STATE
+    m[0, 1] = np.float32(np.inf)
+    assert oracle.check_state(m, v, rows=np.array([0])) == oracle.ERR_BAD_STATE
+    assert oracle.check_state(m, v, rows=np.array([4])) == oracle.ERR_INDEX_OUT_OF_RANGE
+    assert oracle.check_state(m, v, rows=np.array([-1])) == oracle.ERR_INDEX_OUT_OF_RANGE
+    assert oracle.check_state(m, v, rows=np.zeros(0, np.int64)) == oracle.OK
+    # 1-D parameter
+    m1, v1 = np.zeros(5, np.float32), np.ones(5, np.float32)
+    v1[4] = np.nan
+    assert oracle.check_state(m1, v1, rows=np.array([0, 3])) == oracle.OK
+    assert oracle.check_state(m1, v1, rows=np.array([4])) == oracle.ERR_BAD_STATE
