@@ -29,12 +29,19 @@
  *             synchronises the host.  The library's kernels are launched with
  *             programmatic dependent launch: each may be scheduled while the
  *             kernel before it on the stream finishes, and waits for it before
- *             touching memory that kernel may use.  One exception: on a raw
- *             (non-canonical) gradient, the first kernel reads the index array
- *             before that wait, so an index array produced on the same stream
- *             must not be written by a kernel that itself lets its dependents
- *             start early (copies, ordinary kernel launches and this library's
- *             own calls are all fine).
+ *             touching memory that kernel may use.  One read comes earlier: on a
+ *             raw (non-canonical) gradient, the first kernel reads the index
+ *             array before that wait.  That is safe when the index array was
+ *             written by a copy, a memset, an ordinary kernel launch, or any call
+ *             of this library: every call that writes an output other than
+ *             optimizer state and the error word (canonical indices, offsets,
+ *             permutation, linear indices, converted structures, summed or
+ *             gathered values) lets the next kernel start only after those
+ *             writes.  It is not safe when the index array was written by a
+ *             kernel of the caller's own that releases its dependents early
+ *             (programmatic dependent launch), nor when an optimizer state array
+ *             (p, m, v, buf, last_step) of one call is the index array of the
+ *             next call on the same stream.
  *   Errors.   Host-checkable problems (null pointer, negative size, bad config,
  *             t < 1, workspace too small, a size beyond a stated limit) return a
  *             non-zero sparse_status_t before anything is enqueued.  A failed
@@ -83,7 +90,9 @@ typedef enum {
     SPARSE_ERR_WORKSPACE = 5,          /* host: ws missing, misaligned or too small */
     SPARSE_ERR_CUDA = 6,               /* host: a CUDA launch or runtime call failed */
     SPARSE_ERR_INTERNAL = 7,           /* device: a bounded wait between thread blocks gave up */
-    SPARSE_ERR_NON_FINITE = 8          /* device: a gradient value is NaN or infinite (sparse_check_finite) */
+    SPARSE_ERR_NON_FINITE = 8,         /* device: a gradient value is NaN or infinite (sparse_check_finite) */
+    SPARSE_ERR_BAD_STATE = 9           /* device: a touched m is NaN/infinite or a touched v is NaN/infinite/negative
+                                          (sparse_check_state) */
 } sparse_status_t;
 
 /* "Lazy Adam": LazyAdamMode::Lazy and LazyAdamMode::DormancyDecay. */
@@ -255,6 +264,29 @@ sparse_status_t sparse_sgd_table_step(float* p, float* buf, int64_t r, int64_t c
 sparse_status_t sparse_check_finite(const float* vals, int64_t n, int32_t* d_err, cudaStream_t stream);
 
 /*
+ * sparse_check_state -- optional validation of the Adam moments a step would
+ * read ("DiskSparseAdam (DSA)" README, "Validated Inputs": NaN or negative
+ * moment rows have explicit behaviour; here they are an explicit error).
+ *   m, v:  the Adam moments of an (r, c) table (r*c fp32 each; c = 1 for a 1-D
+ *          parameter of dim = r values).
+ *   grad:  the gradient of the step about to run (host struct, device arrays),
+ *          in either form.  ROW_COO: every column of each listed row, in any
+ *          order, repeats allowed (is_canonical is ignored; a row outside [0, r)
+ *          sets SPARSE_ERR_INDEX_OUT_OF_RANGE).  CSR: the listed (row, column)
+ *          coordinates; the structure is validated as by the step.
+ *   A touched m that is NaN or infinite, or a touched v that is NaN, infinite or
+ *   below zero (-0.0 is not below zero) sets *d_err = SPARSE_ERR_BAD_STATE.
+ *   Untouched coordinates are not read; nothing but *d_err is written.
+ *   Enqueued before a step on the same stream with the same d_err, it makes that
+ *   step write no state when a moment it would read is corrupted (the error word
+ *   is sticky).  Without it, a step reads such moments as IEEE values.
+ *   Reads 8 bytes per touched coordinate (per listed row for ROW_COO: repeats
+ *   are read again, mostly from L2); n = 0 is a no-op.
+ */
+sparse_status_t sparse_check_state(const float* m, const float* v, int64_t r, int64_t c, const sparse_grad_t* grad,
+                                   int32_t* d_err, cudaStream_t stream);
+
+/*
  * sparse_read_rows -- the rows of a table at the given indices ("DiskSparseAdam
  * (DSA)" README, API read_rows(indices): the lookup that feeds the forward pass,
  * indices validated).
@@ -280,11 +312,16 @@ sparse_status_t sparse_read_rows(const float* table, int64_t r, int64_t c, const
  *   Arguments, outputs, results and errors are those of sparse_canonicalize,
  *   without ws / ws_bytes.  Inputs and outputs are still caller memory.
  *   Limit: the call needs sparse_workspace_size(n, c, bound) <= SPARSE_STATIC_WS_BYTES
- *   (for example n <= 65,536 entries with c <= 256 columns); larger calls return
+ *   (for example, 65,536 entries of 256 columns fit; the exact limit depends on
+ *   n, c and bound); larger calls return
  *   SPARSE_ERR_WORKSPACE before anything is enqueued.
- *   Set-up: the first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current) and caches it; make that
- *   first call before any stream capture.
+ *   Set-up: every call looks up the array's device address on the current
+ *   device (cudaGetSymbolAddress, with that device current); nothing is cached,
+ *   so a device reset or a re-created primary context is picked up.  Under
+ *   CUDA's lazy module loading the array itself is created by the first call on
+ *   each device (when the library's device code is loaded there): that first
+ *   call can fail with SPARSE_ERR_CUDA on a device with no free memory, so make
+ *   it at set-up time, before any stream capture; later calls allocate nothing.
  *   Sharing: every call uses the same array, which keeps the previous call's
  *   contents (each call clears what it needs cleared).  Calls whose work
  *   overlaps on the GPU -- on different streams, or from different host threads

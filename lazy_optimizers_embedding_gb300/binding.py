@@ -24,6 +24,7 @@ ERR_WORKSPACE = 5
 ERR_CUDA = 6
 ERR_INTERNAL = 7
 ERR_NON_FINITE = 8
+ERR_BAD_STATE = 9
 
 LAZY = 0
 DORMANCY_DECAY = 1
@@ -80,6 +81,7 @@ def _load():
         "sparse_canonicalize_static_ws": (INT, [P, P, I64, I64, I64, P, P, P, P, P, P, P]),
         "sparse_read_rows": (INT, [P, I64, I64, P, I64, P, P, P]),
         "sparse_check_finite": (INT, [P, I64, P, P]),
+        "sparse_check_state": (INT, [P, P, I64, I64, ctypes.POINTER(Grad), P, P]),
         "sparse_profile_enable": (None, [INT]),
         "sparse_profile_reset": (None, []),
         "sparse_profile_read": (INT, [INT, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_int64),
@@ -96,7 +98,8 @@ LIB = _load()
 EXPORTED = ("sparse_workspace_size", "sparse_status_string", "sparse_canonicalize", "sparse_csr_to_coo",
             "sparse_coo_to_csr", "sparse_row_coo_to_csr", "sparse_adam_step", "sparse_adam_table_step",
             "sparse_sgd_step", "sparse_sgd_table_step", "sparse_canonicalize_static_ws", "sparse_profile_enable",
-            "sparse_profile_reset", "sparse_profile_read", "sparse_read_rows", "sparse_check_finite")
+            "sparse_profile_reset", "sparse_profile_read", "sparse_read_rows", "sparse_check_finite",
+            "sparse_check_state")
 STATIC_WS_BYTES = 16 * 1024 * 1024  # SPARSE_STATIC_WS_BYTES
 
 
@@ -262,6 +265,11 @@ def sparse_sgd_table_step(p, buf, r, c, grad: Grad, cfg: SgdConfig, ws, d_err, s
 def sparse_check_finite(vals, n, d_err, stream=None) -> int:
     return LIB.sparse_check_finite(_ptr(vals, torch.float32, "vals"), int(n), _ptr(d_err, torch.int32, "d_err"),
                                    _stream(stream))
+
+
+def sparse_check_state(m, v, r, c, grad: Grad, d_err, stream=None) -> int:
+    return LIB.sparse_check_state(_ptr(m, torch.float32, "m"), _ptr(v, torch.float32, "v"), int(r), int(c),
+                                  ctypes.byref(grad), _ptr(d_err, torch.int32, "d_err"), _stream(stream))
 
 
 def sparse_read_rows(table, r, c, idx, n, out, d_err, stream=None) -> int:

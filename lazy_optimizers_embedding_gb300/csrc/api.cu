@@ -73,7 +73,6 @@ SgdParams sgd_params(float* p, float* buf, const sparse_sgd_config_t& cfg)
     P.momentum_lo = static_cast<float>(cfg.momentum - static_cast<double>(P.momentum));
     P.wd = static_cast<float>(cfg.weight_decay);
     P.wd_lo = static_cast<float>(cfg.weight_decay - static_cast<double>(P.wd));
-    P.wd_lo = static_cast<float>(cfg.weight_decay - static_cast<double>(P.wd));
     return P;
 }
 
@@ -127,6 +126,7 @@ const char* sparse_status_string(sparse_status_t status)
     case SPARSE_ERR_CUDA: return "CUDA error";
     case SPARSE_ERR_INTERNAL: return "internal: a bounded device wait gave up";
     case SPARSE_ERR_NON_FINITE: return "a gradient value is NaN or infinite";
+    case SPARSE_ERR_BAD_STATE: return "a touched moment is NaN or infinite, or a touched second moment is negative";
     }
     return "unknown status";
 }
@@ -301,6 +301,22 @@ sparse_status_t sparse_check_finite(const float* vals, int64_t n, int32_t* d_err
 {
     if (n < 0 || d_err == nullptr || (n > 0 && vals == nullptr)) return SPARSE_ERR_INVALID_ARG;
     return from_cuda(check_finite(vals, n, d_err, stream));
+}
+
+sparse_status_t sparse_check_state(const float* m, const float* v, int64_t r, int64_t c, const sparse_grad_t* grad,
+                                   int32_t* d_err, cudaStream_t stream)
+{
+    sparse_status_t st = check_grad(grad, r, c);
+    if (st) return st;
+    if (d_err == nullptr || (r > 0 && (m == nullptr || v == nullptr))) return SPARSE_ERR_INVALID_ARG;
+    const int64_t n = grad->n;
+    if (grad->form == SPARSE_GRAD_CSR) {
+        cudaError_t e = csr_check(grad->row_off, grad->cols, r, c, n, 0, nullptr, 0, 0, d_err, stream);
+        if (e == cudaSuccess && n > 0) e = check_state_csr(grad->row_off, grad->cols, r, c, n, m, v, d_err, stream);
+        return from_cuda(e);
+    }
+    const int vec4 = (c % 4 == 0) && aligned16(m) && aligned16(v);
+    return from_cuda(check_state_rows(m, v, r, c, grad->row_idx, n, vec4, d_err, stream));
 }
 
 sparse_status_t sparse_read_rows(const float* table, int64_t r, int64_t c, const int64_t* idx, int64_t n, float* out,

@@ -14,17 +14,23 @@ namespace so {
 
 // ---------------------------------------------------------------- launches
 // Every kernel of this library is launched with programmatic dependent launch
-// allowed, and every kernel calls pdl_enter() before it touches memory another
-// kernel uses (at its start, except the histogram kernel, which first counts
-// the caller's index array): it waits until the previous kernel on the stream
-// has completed and its memory is visible (griddepcontrol.wait), then lets the
-// next kernel's blocks be scheduled (griddepcontrol.launch_dependents).  Results and stream order are those of
-// plain launches; what is saved is the launch latency between dependent
-// kernels, since the next grid is already resident when the wait returns.
+// allowed.  A kernel waits (griddepcontrol.wait) until the previous kernel on
+// the stream has completed and its memory is visible before it touches memory
+// another kernel uses; the histogram kernel alone first counts the caller's
+// index array.  Then it lets the next kernel's blocks be scheduled
+// (griddepcontrol.launch_dependents), so that the next grid is resident when
+// this one completes.  A kernel that writes an output the caller may pass as
+// the index array of the next call (canonical indices, offsets, permutation,
+// linear indices, converted structures, gathered or summed values) skips that
+// early release: its dependents start only once all its blocks have exited, so
+// the histogram kernel's early read of an index array never precedes the write.
+// Results and stream order are those of plain launches.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_enter()
 {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_wait();
+    pdl_release();
 }
 
 template <class... P, class... A>
@@ -300,6 +306,10 @@ cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, in
 cudaError_t read_rows(const float* table, int64_t r, int64_t c, const int64_t* idx, int64_t n, float* out, int vec4,
                       int32_t* d_err, cudaStream_t s);
 cudaError_t check_finite(const float* vals, int64_t n, int32_t* d_err, cudaStream_t s);
+cudaError_t check_state_rows(const float* m, const float* v, int64_t r, int64_t c, const int64_t* idx, int64_t n,
+                             int vec4, int32_t* d_err, cudaStream_t s);
+cudaError_t check_state_csr(const int64_t* row_off, const int32_t* cols, int64_t r, int64_t c, int64_t nnz,
+                            const float* m, const float* v, int32_t* d_err, cudaStream_t s);
 cudaError_t csr_adam(const int64_t* row_off, const int32_t* cols, const float* vals, int64_t r,
                      int64_t c, int64_t nnz, const AdamParams& P, int32_t* d_err, cudaStream_t s);
 cudaError_t csr_sgd(const int64_t* row_off, const int32_t* cols, const float* vals, int64_t r,

@@ -438,12 +438,56 @@ cudaError_t csr_sgd(const int64_t* row_off, const int32_t* cols, const float* va
     return cudaGetLastError();
 }
 
+// Moment state at the listed coordinates of a CSR gradient (the step's read
+// set): m not finite, or v not finite or below zero, sets SPARSE_ERR_BAD_STATE.
+// Runs after the structure check on the same error word and does nothing once
+// that word is set, so it never follows malformed offsets or columns.
+__global__ void __launch_bounds__(kBlock) k_check_state_csr(const int64_t* __restrict__ row_off,
+                                                            const int32_t* __restrict__ cols, int64_t r, int64_t c,
+                                                            int64_t nnz, const float* __restrict__ m,
+                                                            const float* __restrict__ v, int32_t* d_err)
+{
+    pdl_enter();
+    if (read_error(d_err)) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t groups = (r + 31) / 32;
+    const int64_t gstride = static_cast<int64_t>(gridDim.x) * (kBlock / 32);
+    bool bad = false;
+    for (int64_t gi = static_cast<int64_t>(blockIdx.x) * (kBlock / 32) + threadIdx.x / 32; gi < groups;
+         gi += gstride) {
+        const int64_t r0 = gi * 32;
+        const Group G = load_group(row_off, r, nnz, r0, lane);
+        if (!G.ok) continue;
+        for (int64_t base = G.lo; base < G.hi; base += 32) {
+            const int64_t j = base + lane;
+            const int l = row_lane(G, j);
+            if (j < G.hi) {
+                const int64_t col = cols[j];
+                if (col >= 0 && col < c) {
+                    const int64_t i = (r0 + l) * c + col;
+                    const float mv = m[i], vv = v[i];
+                    bad |= !isfinite(mv) || !isfinite(vv) || vv < 0.0f;
+                }
+            }
+        }
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) set_error(d_err, SPARSE_ERR_BAD_STATE);
+}
+
+cudaError_t check_state_csr(const int64_t* row_off, const int32_t* cols, int64_t r, int64_t c, int64_t nnz,
+                            const float* m, const float* v, int32_t* d_err, cudaStream_t s)
+{
+    SO_PROFILE("check_state_csr", s);
+    launch(k_check_state_csr, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, r, c, nnz, m, v, d_err);
+    return cudaGetLastError();
+}
+
 // CsrGradient::to_coo: lin[j] = row(j)*c + cols[j].
 __global__ void __launch_bounds__(kBlock) k_csr_to_coo(const int64_t* __restrict__ row_off,
                                                        const int32_t* __restrict__ cols, int64_t r, int64_t c,
                                                        int64_t nnz, int64_t* __restrict__ lin, int32_t* d_err)
 {
-    pdl_enter();
+    pdl_wait();   // writes a caller output: dependents start after this grid exits
     if (read_error(d_err)) return;
     const int lane = threadIdx.x & 31;
     const int64_t groups = (r + 31) / 32;
@@ -494,7 +538,7 @@ __global__ void __launch_bounds__(kBlock) k_merge_offsets(const int64_t* __restr
                                                           int64_t* __restrict__ row_off,
                                                           int32_t* __restrict__ cols, int32_t* d_err)
 {
-    pdl_enter();
+    pdl_wait();   // writes caller outputs: dependents start after this grid exits
     if (read_error(d_err)) return;
     const int64_t total = r + 1 + nb;
     const int64_t d0 = (static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x) * kMergeItems;
@@ -523,7 +567,7 @@ __global__ void __launch_bounds__(kBlock) k_merge_offsets(const int64_t* __restr
 __global__ void __launch_bounds__(kBlock) k_fill_cols(int32_t* __restrict__ cols, int64_t total, int64_t c,
                                                       int32_t* d_err)
 {
-    pdl_enter();
+    pdl_wait();   // writes a caller output: dependents start after this grid exits
     if (read_error(d_err)) return;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; e < total; e += stride)

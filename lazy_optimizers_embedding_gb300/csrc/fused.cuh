@@ -307,6 +307,7 @@ struct AdamEpi {
     static constexpr const char* kName = "fused_rows_adam";
     static constexpr const char* kCombineName = "combine_split_adam";
     static constexpr int kArrays = 3;   // p, m, v
+    static constexpr bool kEarlyRelease = true;   // writes optimizer state only
     AdamParams P;
     int64_t c;
     struct Row {
@@ -355,6 +356,7 @@ struct SgdEpi {
     static constexpr const char* kName = "fused_rows_sgd";
     static constexpr const char* kCombineName = "combine_split_sgd";
     static constexpr int kArrays = 2;   // p, momentum buffer (absent without momentum)
+    static constexpr bool kEarlyRelease = true;   // writes optimizer state only
     SgdParams P;
     int64_t c;
     struct Row {
@@ -382,6 +384,7 @@ struct StoreEpi {
     static constexpr const char* kName = "fused_rows_sum";
     static constexpr const char* kCombineName = "combine_split_sum";
     static constexpr int kArrays = 1;   // no state; one dummy array keeps the types simple
+    static constexpr bool kEarlyRelease = false;  // writes a caller output (the summed rows)
     StoreParams P;
     int64_t c;
     struct Row {
@@ -761,7 +764,8 @@ __global__ void __launch_bounds__(kRowBlock, kFusedMinBlocks) k_fused_rows(Src s
                                                                         int64_t c, Epi epi, float* __restrict__ part,
                                                                         int64_t nb, int32_t* d_err)
 {
-    pdl_enter();
+    pdl_wait();
+    if constexpr (Epi::kEarlyRelease) pdl_release();
     if (read_error(d_err)) return;
     constexpr int kTeams = kRowBlock / T;
     const int lane = threadIdx.x & 31;
@@ -905,7 +909,8 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_split(Src src, int64_
                                                                  float* __restrict__ part, int64_t nb,
                                                                  int32_t* d_err)
 {
-    pdl_enter();
+    pdl_wait();
+    if constexpr (Epi::kEarlyRelease) pdl_release();
     if (read_error(d_err)) return;
     constexpr int kTeams = kCombineBlock / T;
     constexpr int CW = T * NV * V;

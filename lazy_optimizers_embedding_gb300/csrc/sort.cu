@@ -380,7 +380,10 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     const int64_t* __restrict__ ls, int ls_per_coord, int64_t c, int64_t bound, int64_t t,
     int32_t* d_err)
 {
-    pdl_enter();
+    pdl_wait();
+    // canonical outputs are caller memory the next call may read as its index
+    // array: with any of them requested, dependents start after this grid exits
+    if (idx_out == nullptr && seg_off_out == nullptr && perm_out == nullptr && d_nnz_out == nullptr) pdl_release();
     constexpr unsigned long long kValMask = (1ull << 62) - 1ull;
     __shared__ uint32_t s_scan[kBlock / 32 + 1];
     __shared__ unsigned long long s_excl;

@@ -10,34 +10,17 @@
 // the process exits.  The call allocates nothing.
 //
 // Host code cannot use the array's name as a device pointer (in host code it
-// names a host-side shadow), so the device address is looked up once per device
-// with cudaGetSymbolAddress, with that device current, and cached.
-#include <mutex>
-
+// names a host-side shadow), so every call looks up the array's device address
+// on the current device with cudaGetSymbolAddress.  The address is not cached:
+// a cached one would go stale if the device's primary context were torn down
+// and re-created (cudaDeviceReset), and the lookup is cheap once the module is
+// loaded.  Under lazy module loading the first lookup on a device is what loads
+// the library's device code there, and with it creates the array.
 #include "common.cuh"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_static_ws[SPARSE_STATIC_WS_BYTES];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
-
-// Device address of g_static_ws on the current device (looked up on first use).
-sparse_status_t static_ws_address(void** out)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPARSE_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || p == nullptr) return SPARSE_ERR_CUDA;
-        g_addr[dev] = p;
-    }
-    *out = g_addr[dev];
-    return SPARSE_OK;
-}
 
 }  // namespace
 
@@ -50,8 +33,7 @@ extern "C" sparse_status_t sparse_canonicalize_static_ws(const int64_t* idx, con
     if (sparse_workspace_size(n, c, bound) > static_cast<size_t>(SPARSE_STATIC_WS_BYTES))
         return SPARSE_ERR_WORKSPACE;
     void* ws = nullptr;
-    const sparse_status_t st = static_ws_address(&ws);
-    if (st) return st;
+    if (cudaGetSymbolAddress(&ws, g_static_ws) != cudaSuccess || ws == nullptr) return SPARSE_ERR_CUDA;
     return sparse_canonicalize(idx, vals, n, c, bound, idx_out, vals_out, seg_off_out, perm_out, d_nnz_out, ws,
                                static_cast<size_t>(SPARSE_STATIC_WS_BYTES), d_err, stream);
 }

@@ -45,3 +45,14 @@ def cuda_lib():
     __graft_entry__.build()
     from lazy_optimizers_embedding_gb300 import binding
     return binding
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The largest no-floor moment errors the GPU parity tests measured (see gpu_harness)."""
+    h = sys.modules.get("gpu_harness")
+    if h is None or not getattr(h, "DIAG", None):
+        return
+    terminalreporter.section("parity diagnostics (largest errors seen)")
+    for key in sorted(h.DIAG):
+        vals = ", ".join(f"{q} {v:.3e}" for q, v in sorted(h.DIAG[key].items()))
+        terminalreporter.write_line(f"{key}: {vals}")

@@ -5,11 +5,14 @@ still span several radix / run-detection tiles (2,048 entries each), several
 pieces of 32 sorted entries, a ragged tail, and hot keys with enough duplicates
 to need two levels of the partial-combining tree (> 32*32 entries of one key).
 """
+import os
+
 import numpy as np
 import pytest
 
 import oracle
-from gpu_harness import assert_state_close, dev, host, max_rel, tol_violations
+from gpu_harness import (Guarded, MomentScale, assert_m_scaled, assert_state_close, assert_v_relative, dev, host,
+                         max_rel, plant_specials, tol_violations)
 
 pytestmark = pytest.mark.gpu
 
@@ -51,18 +54,20 @@ def test_canonicalize_matches_oracle(cuda_lib, n, c, bound, hot):
     vals[rng.integers(0, n, max(1, n // 50))] = -0.0
     ri, rv, rseg, rperm = oracle.canonicalize(idx, vals, bound)
     u = ri.shape[0]
-    d_idx = dev(idx)
-    d_vals = dev(vals)
-    idx_out = torch.empty(n, dtype=torch.int64, device="cuda")
-    vals_out = torch.empty((n, c), dtype=torch.float32, device="cuda")
-    seg_out = torch.empty(n + 1, dtype=torch.int64, device="cuda")
-    perm_out = torch.empty(n, dtype=torch.int64, device="cuda")
-    nnz = torch.zeros(1, dtype=torch.int64, device="cuda")
-    ws = so.workspace(n, c, bound)
-    err = so.error_word()
+    G = Guarded(seed=n + c)
+    d_idx = G.array(idx)
+    d_vals = G.array(vals)
+    idx_out = G.empty(n, torch.int64)
+    vals_out = G.empty((n, c), torch.float32)
+    seg_out = G.empty(n + 1, torch.int64)
+    perm_out = G.empty(n, torch.int64)
+    nnz = G.zeros(1, torch.int64)
+    ws = G.workspace(so, n, c, bound)
+    err = G.error_word()
     so.check(so.sparse_canonicalize(d_idx, d_vals, n, c, bound, idx_out, vals_out, seg_out, perm_out, nnz, ws,
                                     err), "canonicalize")
-    torch.cuda.synchronize()
+    G.check("canonicalize")
+    assert host(d_idx).tobytes() == idx.tobytes() and host(d_vals).tobytes() == vals.tobytes(), "inputs changed"
     assert int(err.item()) == 0
     assert int(nnz.item()) == u
     assert np.array_equal(host(idx_out)[:u], ri)
@@ -106,53 +111,83 @@ def test_canonicalize_empty_and_deterministic(cuda_lib):
 
 
 # ------------------------------------------------------------------ lazy Adam, raw row-COO
+def _test_key():
+    return os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0].split("::")[-1]
+
+
 def _run_adam(so, R, c, steps, mode, gen, form, layout=None, hp=ADAM, check_every=False):
-    """gen(step) -> gradient for the step, in the given form; runs GPU and oracle side by side."""
+    """gen(step) -> gradient for the step, in the given form; runs GPU and oracle side by side.
+
+    Every device array is guarded (canaries checked after each step); coordinates that no step
+    touches hold planted specials in p, m, v (and large or negative values in last_step) and
+    must come back bit for bit; touched m and v are held to the no-floor checks of gpu_harness."""
     import torch
+    key = _test_key()
     rng = np.random.default_rng(R + c)
-    p0 = (rng.standard_normal((R, c)) * 0.01).astype(np.float32)
+    grads = [gen(s) for s in range(steps)]
     per_coord = layout == so.LAST_STEP_PER_COORD
     ls_n = R * c if per_coord else R
-    p, m, v = dev(p0), torch.zeros((R, c), device="cuda"), torch.zeros((R, c), device="cuda")
-    ls = torch.zeros(ls_n, dtype=torch.int64, device="cuda")
-    op, om, ov, ols = p0.copy(), np.zeros_like(p0), np.zeros_like(p0), np.zeros(ls_n, np.int64)
-    err = so.error_word()
+    ever = np.zeros((R, c), bool)
+    for g in grads:
+        if form in ("raw", "canon"):
+            ever[np.unique(g[0])] = True
+        else:
+            ever[np.repeat(np.arange(R), np.diff(g[0])), g[1]] = True
+    p0 = (rng.standard_normal((R, c)) * 0.01).astype(np.float32)
+    m0, v0 = np.zeros_like(p0), np.zeros_like(p0)
+    srng = np.random.default_rng(99)
+    for a in (p0, m0, v0):
+        plant_specials(a, ~ever, srng)
+    ls0 = np.zeros(ls_n, np.int64)
+    ls_never = ~ever.reshape(-1) if per_coord else ~ever.any(axis=1)
+    pick = np.flatnonzero(ls_never)[:16]
+    ls0[pick] = np.where(np.arange(pick.size) % 2 == 0, np.int64(1) << 40, -5)
+    G = Guarded(seed=R * 7 + c)
+    p, m, v, ls = G.array(p0), G.array(m0), G.array(v0), G.array(ls0)
+    op, om, ov, ols = p0.copy(), m0.copy(), v0.copy(), ls0.copy()
+    err = G.error_word()
     cfg = so.AdamConfig(**hp)
     ohp = dict(hp)   # the oracle names the weight-decay mode wd_mode
     if "weight_decay_mode" in ohp:
         ohp["wd_mode"] = ohp.pop("weight_decay_mode")
     omode = oracle.MODE_DORMANCY_DECAY if mode == so.DORMANCY_DECAY else oracle.MODE_LAZY
+    scale = MomentScale((R, c), ls_n, ohp, omode, per_coord)
     touched = np.zeros((R, c), bool)
     ws = None
     for s in range(steps):
         t = s + 1
-        g = gen(s)
+        g = grads[s]
+        p_before = op.copy()
         if form == "raw" or form == "canon":
             rows, vals = g
             if ws is None and form == "raw":
-                ws = so.workspace(max(rows.shape[0], 1), c, R)
-            grad = so.row_coo(dev(rows), dev(vals), form == "canon")
+                ws = G.workspace(so, max(rows.shape[0], 1), c, R)
+            grad = so.row_coo(G.array(rows), G.array(vals), form == "canon")
             so.check(so.sparse_adam_table_step(p, m, v, ls, layout or so.LAST_STEP_PER_ROW, R, c, grad, t, cfg, mode,
                                                ws, err), "adam_table_step")
             rc = oracle.adam_table_step(op, om, ov, ols, t, rows=rows, vals=vals, is_canonical=(form == "canon"),
                                         mode=omode, ls_per_coord=per_coord, **ohp)
+            scale.step(t, p_before, rows=rows, vals=vals, is_canonical=(form == "canon"))
             touched[np.unique(rows)] = True
         else:
             row_off, cols, vals = g
-            grad = so.csr(dev(row_off), dev(cols), dev(vals))
+            grad = so.csr(G.array(row_off), G.array(cols), G.array(vals))
             so.check(so.sparse_adam_table_step(p, m, v, ls, layout, R, c, grad, t, cfg, mode, None, err),
                      "adam_table_step csr")
             rc = oracle.adam_table_step(op, om, ov, ols, t, row_off=row_off, cols=cols, vals=vals, mode=omode,
                                         ls_per_coord=per_coord, **ohp)
+            scale.step(t, p_before, row_off=row_off, cols=cols, vals=vals)
             rr = np.repeat(np.arange(R), np.diff(row_off))
             touched[rr, cols] = True
         assert rc == 0
-        torch.cuda.synchronize()
+        G.check(f"step {t}")
         assert int(err.item()) == 0, so.status_string(int(err.item()))
         if check_every or s == steps - 1:
             assert_state_close(f"p@t={t}", host(p), op, touched, p0)
-            assert_state_close(f"m@t={t}", host(m), om)
-            assert_state_close(f"v@t={t}", host(v), ov)
+            assert_state_close(f"m@t={t}", host(m), om, touched, m0)
+            assert_state_close(f"v@t={t}", host(v), ov, touched, v0)
+            assert_v_relative(key, f"v@t={t}", host(v), ov, touched)
+            assert_m_scaled(key, f"m@t={t}", host(m), om, scale.M, touched)
             assert np.array_equal(host(ls), ols), f"last_step@t={t}"
     return host(p), host(m), host(v)
 
@@ -366,29 +401,41 @@ def test_adam_1d(cuda_lib, mode, canonical):
                                         (4000, 6, 0.5, 0.1)])
 def test_sgd_raw_rows(cuda_lib, R, c, mom, wd):
     so = cuda_lib
-    import torch
     rng = np.random.default_rng(R + c)
-    p0 = (rng.standard_normal((R, c)) * 0.01).astype(np.float32)
-    p = dev(p0)
-    buf = torch.zeros_like(p) if mom else None
-    op, ob = p0.copy(), np.zeros_like(p0)
-    err = so.error_word()
-    cfg = so.SgdConfig(lr=0.05, momentum=mom, weight_decay=wd)
     n = 6000
-    ws = so.workspace(n, c, R)
+    steps = [(_raw_rows(rng, n, R, hot=R - 1, hot_count=1100 if s == 2 else 0),
+              rng.standard_normal((n, c)).astype(np.float32)) for s in range(6)]
+    never = np.ones(R, bool)
+    for rows, _ in steps:
+        never[rows] = False
+    never2 = np.repeat(never[:, None], c, 1)
+    p0 = (rng.standard_normal((R, c)) * 0.01).astype(np.float32)
+    b0 = np.zeros_like(p0)
+    srng = np.random.default_rng(5)
+    plant_specials(p0, never2, srng)
+    plant_specials(b0, never2, srng)
+    G = Guarded(seed=R + 3 * c)
+    p = G.array(p0)
+    buf = G.array(b0) if mom else None
+    op, ob = p0.copy(), b0.copy()
+    err = G.error_word()
+    cfg = so.SgdConfig(lr=0.05, momentum=mom, weight_decay=wd)
+    ws = G.workspace(so, n, c, R)
     touched = np.zeros(R, bool)
-    for s in range(6):
-        rows = _raw_rows(rng, n, R, hot=R - 1, hot_count=1100 if s == 2 else 0)
-        vals = rng.standard_normal((n, c)).astype(np.float32)
-        so.check(so.sparse_sgd_table_step(p, buf, R, c, so.row_coo(dev(rows), dev(vals), False), cfg, ws, err))
+    for s, (rows, vals) in enumerate(steps):
+        so.check(so.sparse_sgd_table_step(p, buf, R, c, so.row_coo(G.array(rows), G.array(vals), False), cfg, ws,
+                                          err))
         assert oracle.sgd_table_step(op, ob if mom else None, rows=rows, vals=vals, lr=0.05, momentum=mom,
                                      weight_decay=wd) == 0
         touched[rows] = True
-        torch.cuda.synchronize()
+        G.check(f"sgd step {s + 1}")
     assert int(err.item()) == 0
-    assert_state_close("p", host(p), op, np.repeat(touched[:, None], c, 1), p0)
+    tm = np.repeat(touched[:, None], c, 1)
+    assert_state_close("p", host(p), op, tm, p0)
     if mom:
-        assert_state_close("buf", host(buf), ob)
+        assert_state_close("buf", host(buf), ob, tm, b0)
+    else:
+        assert never.any() or R <= 5000
 
 
 def test_sgd_1d_canonical_and_csr(cuda_lib):
@@ -712,3 +759,199 @@ def test_check_finite_then_step_writes_nothing(cuda_lib):
     assert int(err.item()) == so.ERR_NON_FINITE
     assert host(p).tobytes() == p0.tobytes()
     assert not host(m).any() and not host(v).any() and not host(ls).any()
+
+
+# ------------------------------------------------------------------ moment-state check
+def _state_case(rng, R, c, form):
+    m = (rng.standard_normal((R, c)) * 0.1).astype(np.float32)
+    v = (np.abs(rng.standard_normal((R, c))) * 1e-4).astype(np.float32)
+    if form == "csr":
+        nrows = max(1, R // 3)
+        rows = np.sort(rng.choice(R, nrows, replace=False))
+        k = max(1, c // 3)
+        counts = np.zeros(R, np.int64)
+        counts[rows] = k
+        row_off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+        cols = np.sort(np.argsort(rng.random((nrows, c)), axis=1)[:, :k], axis=1).astype(np.int32).reshape(-1)
+        return m, v, dict(row_off=row_off, cols=cols)
+    rows = rng.integers(0, R, 3 * R).astype(np.int64)
+    rows = rows[rows % 5 != 0]          # rows 0, 5, 10, ... are never listed
+    if form == "canon":
+        rows = np.unique(rows)
+    return m, v, dict(rows=rows)
+
+
+@pytest.mark.parametrize("form", ["raw", "canon", "csr"])
+@pytest.mark.parametrize("R,c", [(1, 1), (100, 1), (300, 4), (500, 64), (200, 128), (90, 300), (64, 7)])
+def test_check_state_matches_oracle(cuda_lib, form, R, c):
+    """sparse_check_state against the oracle, with specials planted inside and outside the read set."""
+    import torch
+    so = cuda_lib
+    rng = np.random.default_rng(R * 13 + c + len(form))
+    m, v, g = _state_case(rng, R, c, form)
+    if "rows" in g:
+        read = np.zeros((R, c), bool)
+        read[g["rows"]] = True
+    else:
+        read = np.zeros((R, c), bool)
+        read[np.repeat(np.arange(R), np.diff(g["row_off"])), g["cols"]] = True
+    cases = [("clean", None, None)]
+    for bits, arr in ((0x7FC00001, "m"), (0x7F800000, "m"), (0xFF800000, "v"), (0x7FC12345, "v"),
+                      (0xBF800000, "v"), (0x80000001, "v"), (0x80000000, "v")):
+        cases.append(("inside", bits, arr))
+        cases.append(("outside", bits, arr))
+    for where, bits, arr in cases:
+        mm, vv = m.copy(), v.copy()
+        if bits is not None:
+            pool = np.flatnonzero(read.reshape(-1) if where == "inside" else ~read.reshape(-1))
+            if pool.size == 0:
+                continue
+            (mm if arr == "m" else vv).reshape(-1).view(np.uint32)[rng.choice(pool)] = bits
+        want = oracle.check_state(mm, vv, **g)
+        G = Guarded(seed=R + c)
+        dm, dv = G.array(mm), G.array(vv)
+        if "rows" in g:
+            grad = so.row_coo(G.array(g["rows"]), G.empty((g["rows"].shape[0], c), torch.float32), form == "canon")
+        else:
+            grad = so.csr(G.array(g["row_off"]), G.array(g["cols"]), G.empty(g["cols"].shape[0], torch.float32))
+        err = G.error_word()
+        so.check(so.sparse_check_state(dm, dv, R, c, grad, err), "check_state")
+        G.check("check_state")
+        assert int(err.item()) == want, (where, hex(bits or 0), arr)
+        assert host(dm).tobytes() == mm.tobytes() and host(dv).tobytes() == vv.tobytes()
+
+
+def test_check_state_bad_index_and_empty(cuda_lib):
+    import torch
+    so = cuda_lib
+    m = torch.zeros((10, 4), device="cuda")
+    v = torch.zeros((10, 4), device="cuda")
+    for rows, want in (([2, 10], so.ERR_INDEX_OUT_OF_RANGE), ([-1], so.ERR_INDEX_OUT_OF_RANGE), ([], so.OK)):
+        r = np.array(rows, np.int64)
+        err = so.error_word()
+        grad = so.row_coo(dev(r) if r.size else torch.zeros(1, dtype=torch.int64, device="cuda"),
+                          torch.zeros((max(r.size, 1), 4), device="cuda"), False)
+        grad.n = r.size
+        so.check(so.sparse_check_state(m, v, 10, 4, grad, err))
+        torch.cuda.synchronize()
+        assert int(err.item()) == want
+    # a malformed CSR is reported by the structure check; the state pass reads nothing
+    err = so.error_word()
+    bad = so.csr(dev(np.array([0] * 10 + [5], np.int64)), dev(np.array([0, 1], np.int32)), torch.zeros(2, device="cuda"))
+    so.check(so.sparse_check_state(m, v, 10, 4, bad, err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == so.ERR_NOT_CANONICAL
+
+
+@pytest.mark.parametrize("form", ["raw", "csr"])
+def test_check_state_then_step_writes_nothing(cuda_lib, form):
+    """A corrupted touched moment found before the step leaves every state array untouched."""
+    import torch
+    so = cuda_lib
+    rng = np.random.default_rng(78)
+    R, c = 400, 32
+    p0 = rng.standard_normal((R, c)).astype(np.float32)
+    m0 = (rng.standard_normal((R, c)) * 1e-3).astype(np.float32)
+    v0 = (np.abs(rng.standard_normal((R, c))) * 1e-6).astype(np.float32)
+    if form == "raw":
+        rows = rng.integers(0, R, 1500)
+        v0[rows[700], 3] = np.float32(-1e-9)
+        grad_np = dict(rows=rows)
+        vals = dev(rng.standard_normal((rows.shape[0], c)).astype(np.float32))
+        grad = so.row_coo(dev(rows), vals, False)
+        layout, ls_n, ws = so.LAST_STEP_PER_ROW, R, so.workspace(rows.shape[0], c, R)
+    else:
+        _, _, grad_np = _state_case(rng, R, c, "csr")
+        first = int(np.flatnonzero(np.diff(grad_np["row_off"]))[0])
+        m0[first, grad_np["cols"][grad_np["row_off"][first]]] = np.float32(np.nan)
+        grad = so.csr(dev(grad_np["row_off"]), dev(grad_np["cols"]),
+                      dev(rng.standard_normal(grad_np["cols"].shape[0]).astype(np.float32)))
+        layout, ls_n, ws = so.LAST_STEP_PER_COORD, R * c, None
+    assert oracle.check_state(m0, v0, **grad_np) == oracle.ERR_BAD_STATE
+    p, m, v = dev(p0), dev(m0), dev(v0)
+    ls = torch.zeros(ls_n, dtype=torch.int64, device="cuda")
+    err = so.error_word()
+    so.check(so.sparse_check_state(m, v, R, c, grad, err), "check_state")
+    so.check(so.sparse_adam_table_step(p, m, v, ls, layout, R, c, grad, 1,
+                                       so.AdamConfig(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8), so.DORMANCY_DECAY,
+                                       ws, err), "step")
+    torch.cuda.synchronize()
+    assert int(err.item()) == so.ERR_BAD_STATE
+    assert host(p).tobytes() == p0.tobytes() and host(m).tobytes() == m0.tobytes()
+    assert host(v).tobytes() == v0.tobytes() and not host(ls).any()
+
+
+# ------------------------------------------------------------------ chained calls, no host sync
+def test_chained_outputs_without_host_sync(cuda_lib):
+    """Library outputs fed straight into the next call on the same stream, no synchronisation:
+    CSR -> COO -> canonicalize(lin), and canonicalize(values not requested) -> raw step on its
+    unique indices.  The second call's first kernel reads its index array before waiting for the
+    previous kernel, so every producer must finish its writes before releasing its dependents."""
+    import torch
+    so = cuda_lib
+    rng = np.random.default_rng(123)
+    iters = 40
+    r, c = 3000, 64
+    cases = []
+    for it in range(iters):
+        k = int(rng.integers(1, 60_000))
+        lin = np.sort(rng.choice(r * c, size=k, replace=False)).astype(np.int64)
+        ro, co = oracle.coo_to_csr(lin, r, c)
+        cases.append((lin, ro, co))
+    err = so.error_word()
+    bufs = []
+    for lin, ro, co in cases:   # every input and output allocated first
+        k = lin.shape[0]
+        bufs.append((k, dev(ro), dev(co), torch.empty(k, dtype=torch.int64, device="cuda"),
+                     [torch.empty(k, dtype=torch.int64, device="cuda") for _ in range(4)],
+                     torch.zeros(1, dtype=torch.int64, device="cuda"), so.workspace(k, 1, r * c)))
+    torch.cuda.synchronize()   # from here on nothing waits on the host
+    outs = []
+    for k, d_ro, d_co, lin_out, chain, nnz, ws in bufs:
+        so.check(so.sparse_csr_to_coo(d_ro, d_co, r, c, k, lin_out, err))
+        src = lin_out
+        for dst in chain:      # each canonical output is the next call's raw input
+            so.check(so.sparse_canonicalize(src, None, k, 1, r * c, dst, None, None, None, nnz, ws, err))
+            src = dst
+        outs.append((lin_out, src, nnz))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for (lin, _, _), (lin_out, idx_out, nnz) in zip(cases, outs):
+        assert np.array_equal(host(lin_out), lin)
+        assert int(nnz.item()) == lin.shape[0]
+        assert np.array_equal(host(idx_out), lin)
+
+    # canonicalize without values -> lazy Adam on the unique rows, raw form
+    R, cc, n = 20_000, 32, 30_000
+    cfg = so.AdamConfig(**ADAM)
+    p0 = (rng.standard_normal((R, cc)) * 0.01).astype(np.float32)
+    p, m, v = dev(p0), torch.zeros((R, cc), device="cuda"), torch.zeros((R, cc), device="cuda")
+    ls = torch.zeros(R, dtype=torch.int64, device="cuda")
+    op, om, ov, ols = p0.copy(), np.zeros_like(p0), np.zeros_like(p0), np.zeros(R, np.int64)
+    steps = []
+    for s in range(12):
+        idx = _raw_rows(rng, n, R, hot=s, hot_count=2000)
+        u = np.unique(idx)
+        vals = (rng.standard_normal((u.shape[0], cc)) * 0.01).astype(np.float32)
+        steps.append((idx, u, vals))
+    dev_in = [(dev(idx), dev(vals), torch.empty(n, dtype=torch.int64, device="cuda")) for idx, _, vals in steps]
+    wsc, wss = so.workspace(n, 1, R), so.workspace(n, cc, R)
+    nnz = torch.zeros(1, dtype=torch.int64, device="cuda")
+    torch.cuda.synchronize()
+    for t, ((idx, u, vals), (d_idx, d_vals, idx_out)) in enumerate(zip(steps, dev_in), start=1):
+        so.check(so.sparse_canonicalize(d_idx, None, n, 1, R, idx_out, None, None, None, nnz, wsc, err))
+        so.check(so.sparse_adam_table_step(p, m, v, ls, so.LAST_STEP_PER_ROW, R, cc,
+                                           so.row_coo(idx_out[:u.shape[0]], d_vals, False), t, cfg,
+                                           so.DORMANCY_DECAY, wss, err))
+        assert u.shape[0] <= n
+    for t, (idx, u, vals) in enumerate(steps, start=1):
+        assert oracle.adam_table_step(op, om, ov, ols, t, rows=u, vals=vals, mode=oracle.MODE_DORMANCY_DECAY,
+                                      **ADAM) == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, so.status_string(int(err.item()))
+    for (idx, u, _), (_, _, idx_out) in zip(steps, dev_in):
+        assert np.array_equal(host(idx_out)[:u.shape[0]], u)
+    assert_state_close("p", host(p), op)
+    assert_state_close("m", host(m), om)
+    assert_state_close("v", host(v), ov)
+    assert np.array_equal(host(ls), ols)

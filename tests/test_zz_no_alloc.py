@@ -79,3 +79,56 @@ def test_static_workspace_rejects_sizes_beyond_its_limit(cuda_lib):
     assert so.sparse_canonicalize_static_ws(idx, vals, n, c, bound, *outs, err) == so.ERR_WORKSPACE
     torch.cuda.synchronize()
     assert int(outs[4].item()) == -1 and int(err.item()) == 0  # nothing was enqueued
+
+
+def _largest_n(so, c, bound):
+    """The largest entry count whose workspace fits the static array (workspace size grows with n)."""
+    lo, hi = 1, 1 << 24
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if so.sparse_workspace_size(mid, c, bound) <= so.STATIC_WS_BYTES:
+            lo = mid
+        else:
+            hi = mid - 1
+    return lo
+
+
+def test_static_workspace_size_boundary(cuda_lib):
+    """The largest call that fits the array is accepted and correct; one entry more is refused."""
+    so = cuda_lib
+    import torch
+    c, bound = 256, 1_000_000
+    n = _largest_n(so, c, bound)
+    assert so.sparse_workspace_size(n + 1, c, bound) > so.STATIC_WS_BYTES
+    rng = np.random.default_rng(21)
+    idx = rng.integers(0, bound, n).astype(np.int64)
+    idx[:2000] = 3
+    vals = rng.standard_normal((n, c)).astype(np.float32)
+    _canonicalize_both(so, torch, idx, vals, bound)
+    d_idx, d_vals = dev(np.zeros(n + 1, np.int64)), dev(np.zeros((n + 1, c), np.float32))
+    outs = _outputs(torch, n + 1, c)
+    err = so.error_word()
+    assert so.sparse_canonicalize_static_ws(d_idx, d_vals, n + 1, c, bound, *outs, err) == so.ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert int(outs[4].item()) == -1 and int(err.item()) == 0
+
+
+def test_static_workspace_allocates_nothing(cuda_lib):
+    """After the first call on the device (which may load the library's device code and so create
+    the array), further calls leave the device's free memory unchanged."""
+    so = cuda_lib
+    import torch
+    rng = np.random.default_rng(22)
+    n, c, bound = 40_000, 32, 5_000
+    d_idx = dev(rng.integers(0, bound, n).astype(np.int64))
+    d_vals = dev(rng.standard_normal((n, c)).astype(np.float32))
+    outs = _outputs(torch, n, c)
+    err = so.error_word()
+    so.check(so.sparse_canonicalize_static_ws(d_idx, d_vals, n, c, bound, *outs, err), "first call")
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        so.check(so.sparse_canonicalize_static_ws(d_idx, d_vals, n, c, bound, *outs, err), "later call")
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert int(err.item()) == 0 and int(outs[4].item()) > 0
