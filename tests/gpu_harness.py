@@ -10,8 +10,9 @@ Tolerances (fp32 state against the fp64 oracle rounded to fp32):
   - m also against the scale its rounding errors live on: |gpu - ref| <= 1e-5 M,
     where M is the same recursion run on magnitudes (M = b1 M + (1-beta1)|g|,
     |g| + wd|p| under L2 weight decay).  m's two terms can cancel, so its
-    error is bounded relative to M, not to |m|; where M <= 1e3 |m| (no heavy
-    cancellation) the plain no-floor relative error is asserted too;
+    error is bounded relative to M, not to |m|; where M <= 10 |m| (at most one
+    decimal digit lost to cancellation) the plain no-floor relative error is
+    asserted too;
   - untouched coordinates (planted NaN payloads, -0.0, denormals, infinities
     included) and last_step bit for bit;
   - every device array sits inside a guard region of seeded canary bytes that
@@ -29,7 +30,7 @@ import oracle
 RTOL = 1e-5
 ATOL = 1e-7
 MOMENT_RTOL = 1e-5     # v relative (no floor) and m relative to its magnitude scale M
-CANCEL = 1e3           # entries with M <= CANCEL*|m| also get the no-floor relative check on m
+CANCEL = 10.0          # entries with M <= CANCEL*|m| also get the no-floor relative check on m
 
 DIAG: dict[str, dict[str, float]] = {}
 
@@ -70,8 +71,8 @@ def max_rel(got, ref):
 
 def assert_v_relative(key, name, got, ref, touched):
     """Second moments: no-floor relative error on touched coordinates; exact zeros stay zero."""
-    g = np.asarray(got, np.float64)[touched]
-    r = np.asarray(ref, np.float64)[touched]
+    g = np.asarray(got)[touched].astype(np.float64)
+    r = np.asarray(ref)[touched].astype(np.float64)
     nz = r != 0
     rel = float(np.max(np.abs(g[nz] - r[nz]) / r[nz])) if nz.any() else 0.0
     note(key, "v max rel (no floor)", rel)
@@ -83,8 +84,8 @@ def assert_v_relative(key, name, got, ref, touched):
 def assert_m_scaled(key, name, got, ref, scale, touched):
     """First moments: error relative to the magnitude scale M, and no-floor relative where
     the recursion did not cancel heavily."""
-    g = np.asarray(got, np.float64)[touched]
-    r = np.asarray(ref, np.float64)[touched]
+    g = np.asarray(got)[touched].astype(np.float64)
+    r = np.asarray(ref)[touched].astype(np.float64)
     M = np.asarray(scale, np.float64)[touched]
     pos = M > 0
     err = np.abs(g - r)
@@ -94,7 +95,7 @@ def assert_m_scaled(key, name, got, ref, scale, touched):
     assert np.all(g[~pos] == r[~pos]), f"{name}: m differs where every gradient was zero"
     well = pos & (np.abs(r) > 0) & (M <= CANCEL * np.abs(r))
     rel = float(np.max(err[well] / np.abs(r[well]))) if well.any() else 0.0
-    note(key, "m max rel (no floor, M <= 1e3|m|)", rel)
+    note(key, "m max rel (no floor, M <= 10|m|)", rel)
     assert rel <= MOMENT_RTOL, f"{name}: max relative error of m {rel:.3e} > {MOMENT_RTOL}"
 
 
