@@ -35,8 +35,8 @@ namespace so {
 // at most 80 registers, 24 warps per SM), short pieces per work ticket
 // (kTicket), gradient rows a lane requests at once (kRowIlp, kLongIlp), rows of
 // a long piece staged in shared memory per round (kLongStage), threads of a
-// combine block and the partial pairs a lane of it requests at once
-// (kCombineIlp).  Overridable at build time for tuning sweeps.
+// combine block and the partial pairs a thread of it requests at once when they
+// are not staged (kCombineIlp).  Overridable at build time for tuning sweeps.
 #ifndef SO_FUSED_MIN_BLOCKS
 #define SO_FUSED_MIN_BLOCKS 3
 #endif
@@ -854,75 +854,124 @@ __global__ void __launch_bounds__(kRowBlock, kFusedMinBlocks) k_fused_rows(Src s
     }
 }
 
-// Merges the partial pairs of pieces piece_of(0), ..., piece_of(cnt-1) of a split
-// segment, in that order, at this lane's columns of the chunk at col0.
-template <int T, int NV, int V, class PieceOf>
-__device__ __forceinline__ void merge_partials(const float* __restrict__ part, int64_t c, int64_t nb,
-                                               const SplitSegment& seg, PieceOf piece_of, int64_t cnt,
-                                               int64_t col0, int tl, float (&S)[NV][V], float (&C)[NV][V])
+// Partial slots of a run of pairs: pair 0 in slot `first`, pair k >= 1 in slot
+// base + k*step (the slots of a split segment's pieces after the first are
+// consecutive, those of its group heads kGroup apart).
+struct SlotRun {
+    int64_t first, base, step, cnt;
+    __device__ __forceinline__ int64_t slot(int64_t k) const { return k == 0 ? first : base + k * step; }
+};
+
+// Columns a combine block merges per round through its shared stage, and the
+// pairs it stages per round: one group's worth, so that merging a group costs
+// one round trip.
+constexpr int kCombineCols = kCombineBlock;
+constexpr int kCombinePairs = kGroup;
+__host__ __device__ constexpr size_t combine_stage_bytes()
 {
-    constexpr int MR = NV >= kCombineIlp ? 1 : kCombineIlp / NV;   // partial pairs requested at once
-    for (int64_t m0 = 0; m0 < cnt; m0 += MR) {
-        float xs[MR][NV][V], xc[MR][NV][V];
-#pragma unroll
-        for (int r = 0; r < MR; ++r) {
-            if (m0 + r < cnt) {
-                const float* ps = part + part_slot(seg.start(piece_of(m0 + r)), nb) * 2 * c;
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                    if (col < c) {
-                        ld_part<V>(ps + col, xs[r][k]);
-                        ld_part<V>(ps + c + col, xc[r][k]);
-                    }
+    return static_cast<size_t>(kCombinePairs) * 2 * kCombineCols * sizeof(float);
+}
+
+// Merges the pairs of `run`, in order, at columns col0 + threadIdx.x (one column
+// per thread, threads past the row's end idle) into (S, C).  The block copies up
+// to kCombinePairs pairs of kCombineCols columns a round into shared memory with
+// 16-byte cp.async (through L2, so pairs other blocks stored and released are
+// seen), then each thread merges its column.  Every thread of the block calls.
+// Needs c % 4 == 0 and a 16-byte aligned partial array.
+__device__ __forceinline__ void merge_staged(const float* __restrict__ part, int64_t c, const SlotRun& run,
+                                             int64_t col0, float* stage, float& S, float& C)
+{
+    const int64_t width = (c - col0) < kCombineCols ? (c - col0) : kCombineCols;   // a multiple of 4
+    const int quads = static_cast<int>(width / 4);
+    const uint32_t st0 = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
+    for (int64_t m0 = 0; m0 < run.cnt; m0 += kCombinePairs) {
+        const int k = (run.cnt - m0) < kCombinePairs ? static_cast<int>(run.cnt - m0) : kCombinePairs;
+        const int copies = k * 2 * quads;
+        for (int e = threadIdx.x; e < copies; e += kCombineBlock) {
+            const int pr = e / (2 * quads);
+            const int rem = e - pr * 2 * quads;
+            const int sc = rem / quads;
+            const int q = rem - sc * quads;
+            const float* src = part + run.slot(m0 + pr) * 2 * c + sc * c + col0 + 4 * q;
+            const uint32_t dst = st0 + static_cast<uint32_t>(((pr * 2 + sc) * kCombineCols + 4 * q) * 4);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+        }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        if (threadIdx.x < width) {
+            for (int r = 0; r < k; ++r) {
+                const float xs = stage[(r * 2) * kCombineCols + threadIdx.x];
+                const float xc = stage[(r * 2 + 1) * kCombineCols + threadIdx.x];
+                if (m0 + r == 0) {
+                    S = xs;
+                    C = xc;
+                } else {
+                    two_sum_merge(S, C, xs, xc);
                 }
             }
         }
+        __syncthreads();   // the stage is reused by the next round
+    }
+}
+
+// The same for one column, pairs loaded into registers kCombineIlp at a time
+// (any c and alignment).
+__device__ __forceinline__ void merge_column(const float* __restrict__ part, int64_t c, const SlotRun& run,
+                                             int64_t col, float& S, float& C)
+{
+    for (int64_t m0 = 0; m0 < run.cnt; m0 += kCombineIlp) {
+        float xs[kCombineIlp], xc[kCombineIlp];
 #pragma unroll
-        for (int r = 0; r < MR; ++r) {
-            if (m0 + r < cnt) {
+        for (int r = 0; r < kCombineIlp; ++r) {
+            if (m0 + r < run.cnt) {
+                const float* q = part + run.slot(m0 + r) * 2 * c + col;
+                xs[r] = __ldcg(q);
+                xc[r] = __ldcg(q + c);
+            }
+        }
 #pragma unroll
-                for (int k = 0; k < NV; ++k)
-#pragma unroll
-                    for (int i = 0; i < V; ++i) {
-                        if (m0 + r == 0) {
-                            S[k][i] = xs[r][k][i];
-                            C[k][i] = xc[r][k][i];
-                        } else {
-                            two_sum_merge(S[k][i], C[k][i], xs[r][k][i], xc[r][k][i]);
-                        }
-                    }
+        for (int r = 0; r < kCombineIlp; ++r) {
+            if (m0 + r < run.cnt) {
+                if (m0 + r == 0) {
+                    S = xs[r];
+                    C = xc[r];
+                } else {
+                    two_sum_merge(S, C, xs[r], xc[r]);
+                }
             }
         }
     }
 }
 
-// The split segments, in one launch: one team per combine group (listed by run
-// detection through its head piece) merges the group's partials in piece order
-// into the head's slot, then counts the group in its segment (atomic counter;
-// the pair is released first); the last group of a segment to arrive merges the
-// groups' pairs in group order and applies the update.  The order of every
-// addition is fixed by the slots, whichever team arrives last, and no team
-// waits for another.
-template <int T, int NV, int V, class Src, class Epi>
-__global__ void __launch_bounds__(kCombineBlock) k_combine_split(Src src, int64_t c, Epi epi,
-                                                                 float* __restrict__ part, int64_t nb,
-                                                                 int32_t* d_err)
+// The split segments, in one launch: one block per combine group (listed by run
+// detection through its head piece), one column per thread.  A segment of one
+// group is merged and updated by that block directly; in a longer one every
+// block merges its group's partials in piece order into the group head's slot
+// and counts the group in its segment (atomic counter; the pair is released
+// first), and the block of the last group to arrive merges the groups' pairs in
+// group order and applies the update.  The order of every addition is fixed by
+// the slots, whichever block arrives last, and no block waits for another.
+// kStaged: pairs staged through shared memory (c % 4 == 0, aligned partials).
+template <class Src, class Epi, bool kStaged>
+__global__ void __launch_bounds__(kCombineBlock, 3) k_combine_split(Src src, int64_t c, Epi epi,
+                                                                    float* __restrict__ part, int64_t nb,
+                                                                    int32_t* d_err)
 {
     pdl_wait();
     if constexpr (Epi::kEarlyRelease) pdl_release();
     if (read_error(d_err)) return;
-    constexpr int kTeams = kCombineBlock / T;
-    constexpr int CW = T * NV * V;
     constexpr int A = Epi::kArrays;
-    const int lane = threadIdx.x & 31;
-    const int tl = lane & (T - 1);
-    const unsigned tmask = (T == 32) ? kFull : (((1u << T) - 1u) << (lane & ~(T - 1)));
-    const int64_t team_g = static_cast<int64_t>(blockIdx.x) * kTeams + threadIdx.x / T;
-    const int64_t nteams = static_cast<int64_t>(gridDim.x) * kTeams;
-    const int nchunks = static_cast<int>((c + CW - 1) / CW);
+    extern __shared__ float so_combine_stage[];
+    __shared__ uint32_t s_arrived;
+    const auto merge = [&](const SlotRun& run, int64_t col0, float& S, float& C) {
+        if constexpr (kStaged) {
+            merge_staged(part, c, run, col0, so_combine_stage, S, C);
+        } else {
+            if (col0 + threadIdx.x < c) merge_column(part, c, run, col0 + threadIdx.x, S, C);
+        }
+    };
     const int64_t G = src.count_groups();
-    for (int64_t t = team_g; t < G; t += nteams) {
+    for (int64_t t = blockIdx.x; t < G; t += gridDim.x) {
         const PieceInfo pc = src.piece(src.group_index(t));
         int64_t s0, s1;
         src.seg_bounds(pc.u(), s0, s1);
@@ -931,55 +980,53 @@ __global__ void __launch_bounds__(kCombineBlock) k_combine_split(Src src, int64_
         const int64_t K = seg.pieces();
         const int64_t next = seg.group_head(seg.group(i) + 1);
         const int64_t cnt = (next < K ? next : K) - i;
-        if (cnt > 1) {
-            float* pd = part + part_slot(pc.start, nb) * 2 * c;
-            for (int cc = 0; cc < nchunks; ++cc) {
-                const int64_t col0 = static_cast<int64_t>(cc) * CW;
-                float S[NV][V], C[NV][V];
-                merge_partials<T, NV, V>(part, c, nb, seg, [i](int64_t k) { return i + k; }, cnt, col0, tl, S, C);
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
+        const int64_t g0 = seg.group(0);
+        const int64_t ng = seg.group(K - 1) - g0 + 1;
+        // this group's pieces: the first in its own slot, piece p >= 1 of the segment
+        // in slot q1/kPieceLen + p - 1; the group heads after the segment's first
+        // piece: group g's in slot g*kGroup
+        const SlotRun pieces{part_slot(pc.start, nb), seg.q1 / kPieceLen + i - 1, 1, cnt};
+        const SlotRun groups{part_slot(s0, nb), g0 * kGroup, kGroup, ng};
+        if (ng > 1) {
+            if (cnt > 1) {
+                float* pd = part + pieces.first * 2 * c;
+                for (int64_t col0 = 0; col0 < c; col0 += kCombineCols) {
+                    float S, C;
+                    merge(pieces, col0, S, C);
+                    const int64_t col = col0 + threadIdx.x;
                     if (col < c) {
-                        st_part<V>(pd + col, S[k]);
-                        st_part<V>(pd + c + col, C[k]);
+                        st_part<1>(pd + col, {S});
+                        st_part<1>(pd + c + col, {C});
                     }
                 }
             }
-        }
-        const int64_t g0 = seg.group(0);
-        const int64_t ng = seg.group(K - 1) - g0 + 1;
-        if (ng > 1) {
             __threadfence();
-            __syncwarp(tmask);
-            uint32_t old = 0;
-            if (tl == 0) old = atomicAdd(src.segment_counter(part_slot(s0, nb)), 1u);
-            old = __shfl_sync(tmask, old, 0, T);
-            if (static_cast<int64_t>(old) != ng - 1) continue;   // another group's team finishes the segment
+            __syncthreads();
+            if (threadIdx.x == 0) s_arrived = atomicAdd(src.segment_counter(groups.first), 1u);
+            __syncthreads();
+            if (static_cast<int64_t>(s_arrived) != ng - 1) continue;   // another group's block finishes it
             __threadfence();
         }
         const int64_t* lp = epi.stage_last(pc);
         const int64_t last = lp ? *lp : 0;
         const typename Epi::Row row = epi.make_row(pc, last);
-        for (int cc = 0; cc < nchunks; ++cc) {
-            const int64_t col0 = static_cast<int64_t>(cc) * CW;
-            float x[NV][A][V];
-            load_state<T, NV, V>(epi, pc, c, col0, tl, x);
-            float S[NV][V], C[NV][V];
-            merge_partials<T, NV, V>(part, c, nb, seg, [&seg, g0](int64_t k) { return seg.group_head(g0 + k); },
-                                     ng, col0, tl, S, C);
+        for (int64_t col0 = 0; col0 < c; col0 += kCombineCols) {
+            const int64_t col = col0 + threadIdx.x;
+            float x[A][1];
+            if (col < c) {
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int64_t col = col0 + static_cast<int64_t>(k * T + tl) * V;
-                if (col < c) {
-                    float g[V];
-#pragma unroll
-                    for (int e = 0; e < V; ++e) g[e] = __fadd_rn(S[k][e], C[k][e]);
-                    epi.template apply<V>(row, col, x[k], g);
-                }
+                for (int a = 0; a < A; ++a)
+                    if (a < epi.arrays()) x[a][0] = epi.array(a)[epi.base(pc) + col];
+            }
+            float S, C;
+            merge(ng > 1 ? groups : pieces, col0, S, C);
+            if (col < c) {
+                const float g[1] = {__fadd_rn(S, C)};
+                epi.template apply<1>(row, col, x, g);
             }
         }
-        epi.end_row(row, tl, tmask);
+        __syncthreads();   // every thread has read the row's last_step before it is rewritten
+        epi.end_row(row, static_cast<int>(threadIdx.x), kFull);
     }
 }
 
@@ -1022,14 +1069,19 @@ cudaError_t launch_shape(const Src& src, int64_t max_pieces, int64_t max_split, 
         if (e != cudaSuccess) return e;
     }
     if (max_split > 0) {
-        constexpr int kCTeams = kCombineBlock / T;
-        static const int occ = max_blocks(k_combine_split<T, NV, V, Src, Epi>, kCombineBlock);
-        const int64_t cap = static_cast<int64_t>(occ) * num_sms();
         SO_PROFILE(Epi::kCombineName, s);
         const int64_t groups = nb + nb / kGroup + 2;   // bound on the combine groups
-        const int64_t gb = std::min<int64_t>(cap, (groups + kCTeams - 1) / kCTeams);
-        launch(k_combine_split<T, NV, V, Src, Epi>, dim3(static_cast<unsigned>(gb)), dim3(kCombineBlock), s, src, c,
-               epi, part, nb, d_err);
+        if (c % 4 == 0 && (reinterpret_cast<uintptr_t>(part) & 15u) == 0) {
+            static const int occ = max_blocks(k_combine_split<Src, Epi, true>, kCombineBlock, combine_stage_bytes());
+            const int64_t gb = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(occ) * num_sms(), groups));
+            launch_smem(k_combine_split<Src, Epi, true>, dim3(static_cast<unsigned>(gb)), dim3(kCombineBlock),
+                        combine_stage_bytes(), s, src, c, epi, part, nb, d_err);
+        } else {
+            static const int occ = max_blocks(k_combine_split<Src, Epi, false>, kCombineBlock);
+            const int64_t gb = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(occ) * num_sms(), groups));
+            launch(k_combine_split<Src, Epi, false>, dim3(static_cast<unsigned>(gb)), dim3(kCombineBlock), s, src, c,
+                   epi, part, nb, d_err);
+        }
         return cudaGetLastError();
     }
     return cudaSuccess;
