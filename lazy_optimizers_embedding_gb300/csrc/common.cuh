@@ -94,7 +94,7 @@ constexpr int kHistItems = 8;          // keys a histogram thread requests at on
 #define SO_HIST_KEYS 8192
 #endif
 #ifndef SO_RADIX_LOOK
-#define SO_RADIX_LOOK 4
+#define SO_RADIX_LOOK 16
 #endif
 constexpr int kMaxHistBlocks = SO_HIST_BLOCKS;     // histogram blocks at most
 constexpr int kHistKeysPerBlock = SO_HIST_KEYS;    // keys per histogram block (fewer blocks for small n)

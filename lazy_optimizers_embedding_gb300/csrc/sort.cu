@@ -426,6 +426,33 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
             piecem |= ((h || split) ? 1u : 0u) << i;
         }
     }
+    // everything the items below read is requested before the scan and the
+    // look-back, whose round trips it then overlaps: input positions, the key at
+    // the next piece boundary of each segment head, last_step
+    uint32_t pmv[kRunItems];
+    if (p0 + kRunItems <= n) {
+#pragma unroll
+        for (int v4 = 0; v4 < kRunItems / 4; ++v4) {
+            const uint4 a = *reinterpret_cast<const uint4*>(sperm + p0 + 4 * v4);
+            pmv[4 * v4] = a.x; pmv[4 * v4 + 1] = a.y; pmv[4 * v4 + 2] = a.z; pmv[4 * v4 + 3] = a.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kRunItems; ++i) pmv[i] = (p0 + i < n) ? sperm[p0 + i] : 0u;
+    }
+    uint32_t nxt_key[kRunItems], long_key[kRunItems];
+    int64_t last[kRunItems];
+#pragma unroll
+    for (int i = 0; i < kRunItems; ++i) {
+        const uint32_t q = p0 + i;
+        const bool h = (headm >> i) & 1u;
+        // first boundary that can split a segment starting at q: the smallest
+        // multiple of kPieceLen that is >= q + kPieceLen
+        const uint32_t nxt = (q + 2 * kPieceLen - 1) / kPieceLen * kPieceLen;
+        nxt_key[i] = (h && nxt < n) ? skey[nxt] : ~k[i];
+        long_key[i] = (h && q + kShortLen < n) ? skey[q + kShortLen] : ~k[i];
+        last[i] = (h && ls && !ls_per_coord && static_cast<int64_t>(k[i]) < bound) ? ls[k[i]] : 0;
+    }
     const uint32_t hc = __popc(headm), pc = __popc(piecem);
     uint32_t tot;
     const uint32_t xe = block_excl_scan((hc << 16) | pc, s_scan, &tot);
@@ -471,32 +498,6 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     uint32_t h_run = static_cast<uint32_t>(ex >> 31) + (xe >> 16);       // heads before p0
     uint32_t p_run = static_cast<uint32_t>(ex & 0x7fffffffull) + (xe & 0xffffu);
 
-    // everything the items below read is requested first: input positions,
-    // the key at the next piece boundary of each segment head, last_step
-    uint32_t pmv[kRunItems];
-    if (p0 + kRunItems <= n) {
-#pragma unroll
-        for (int v4 = 0; v4 < kRunItems / 4; ++v4) {
-            const uint4 a = *reinterpret_cast<const uint4*>(sperm + p0 + 4 * v4);
-            pmv[4 * v4] = a.x; pmv[4 * v4 + 1] = a.y; pmv[4 * v4 + 2] = a.z; pmv[4 * v4 + 3] = a.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < kRunItems; ++i) pmv[i] = (p0 + i < n) ? sperm[p0 + i] : 0u;
-    }
-    uint32_t nxt_key[kRunItems], long_key[kRunItems];
-    int64_t last[kRunItems];
-#pragma unroll
-    for (int i = 0; i < kRunItems; ++i) {
-        const uint32_t q = p0 + i;
-        const bool h = (headm >> i) & 1u;
-        // first boundary that can split a segment starting at q: the smallest
-        // multiple of kPieceLen that is >= q + kPieceLen
-        const uint32_t nxt = (q + 2 * kPieceLen - 1) / kPieceLen * kPieceLen;
-        nxt_key[i] = (h && nxt < n) ? skey[nxt] : ~k[i];
-        long_key[i] = (h && q + kShortLen < n) ? skey[q + kShortLen] : ~k[i];
-        last[i] = (h && ls && !ls_per_coord && static_cast<int64_t>(k[i]) < bound) ? ls[k[i]] : 0;
-    }
     uint32_t lists[kRunItems];   // flagged pieces of this thread, in order
     uint64_t kinds = 0;          // 3 bits per flagged piece: long, split head, group head
     static_assert(3 * kRunItems <= 64, "kinds holds 3 bits per item");
