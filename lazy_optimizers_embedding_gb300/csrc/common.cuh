@@ -74,16 +74,30 @@ constexpr int kBlock = 256;            // threads per block of every kernel here
 #define SO_PIECE_LEN 32
 #endif
 constexpr int kPieceLen = SO_PIECE_LEN;   // L: sorted entries summed by one team before a partial
+// Keys per thread of a radix pass and sorted entries per thread of run detection
+// (a multiple of 4 dividing kPieceLen): kSortItems / kRunItems below kLargeN
+// entries, the large-input sizes from kLargeN on (fewer, larger tiles shorten the
+// look-back chains of large inputs; smaller tiles start more blocks on small ones).
 #ifndef SO_SORT_ITEMS
 #define SO_SORT_ITEMS 8
 #endif
 #ifndef SO_RUN_ITEMS
 #define SO_RUN_ITEMS 8
 #endif
-constexpr int kSortItems = SO_SORT_ITEMS;   // keys per thread in a radix pass
-constexpr int kSortTile = kBlock * kSortItems;
-constexpr int kRunItems = SO_RUN_ITEMS;     // sorted entries per thread in run detection (a multiple of 4)
-constexpr int kRunTile = kBlock * kRunItems;
+#ifndef SO_SORT_ITEMS_LARGE
+#define SO_SORT_ITEMS_LARGE 16
+#endif
+#ifndef SO_RUN_ITEMS_LARGE
+#define SO_RUN_ITEMS_LARGE 16
+#endif
+#ifndef SO_LARGE_N
+#define SO_LARGE_N (1 << 19)
+#endif
+constexpr int kSortItems = SO_SORT_ITEMS;
+constexpr int kRunItems = SO_RUN_ITEMS;
+constexpr int kSortItemsLarge = SO_SORT_ITEMS_LARGE;
+constexpr int kRunItemsLarge = SO_RUN_ITEMS_LARGE;
+constexpr int64_t kLargeN = SO_LARGE_N;
 constexpr int kMaxPasses = 4;          // 8-bit digits, keys < 2^32
 constexpr int kGroup = 32;             // pieces of a split segment merged by one team first
 constexpr int kHistItems = 8;          // keys a histogram thread requests at once
@@ -205,7 +219,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* tmp, u
 // ------------------------------------------------------------ workspace map
 struct WsLayout {
     int64_t n, c, nb;
-    int passes, sort_tiles, run_tiles, hist_blocks;
+    int passes, sort_items, run_items, sort_tiles, run_tiles, hist_blocks;
     size_t keys0, keys1, vals0, vals1, rec, seg_off, mlist, slist, glist, part, bh, gh;
     size_t ctrl_begin, counts, rstatus, dstatus, scnt, ctrl_end;
     size_t total;

@@ -47,8 +47,10 @@ WsLayout ws_layout(int64_t n, int64_t c, int64_t bound)
     L.c = c;
     L.nb = (n + kPieceLen - 1) / kPieceLen;
     L.passes = (key_bits(bound) + 7) / 8;
-    L.sort_tiles = (int)((n + kSortTile - 1) / kSortTile);
-    L.run_tiles = (int)((n + kRunTile - 1) / kRunTile);
+    L.sort_items = n >= kLargeN ? kSortItemsLarge : kSortItems;
+    L.run_items = n >= kLargeN ? kRunItemsLarge : kRunItems;
+    L.sort_tiles = (int)((n + kBlock * L.sort_items - 1) / (kBlock * L.sort_items));
+    L.run_tiles = (int)((n + kBlock * L.run_items - 1) / (kBlock * L.run_items));
     size_t off = 0;
     auto take = [&](size_t bytes) {
         off = align_up(off, 256);
@@ -184,7 +186,7 @@ __device__ __forceinline__ uint32_t sum_hist(const uint32_t* __restrict__ bh, in
 //      (flag 2 = inclusive); status word = count << 2 | flag;
 //   3. the tile is reordered by digit in shared memory and written out, each
 //      digit's run landing contiguously at its global offset.
-template <bool kFirst>
+template <bool kFirst, int SI>
 __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict__ idx64,
                                                        const uint32_t* __restrict__ kin,
                                                        const uint32_t* __restrict__ vin,
@@ -201,8 +203,8 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
     __shared__ uint32_t s_gbase[256];
     __shared__ uint32_t s_texcl[256];
     __shared__ uint32_t s_scan[kWarps + 1];
-    __shared__ uint32_t s_keys[kSortTile];
-    __shared__ uint32_t s_vals[kSortTile];
+    __shared__ uint32_t s_keys[(kBlock * SI)];
+    __shared__ uint32_t s_vals[(kBlock * SI)];
     __shared__ uint32_t s_tile;
 
     const int tid = threadIdx.x;
@@ -212,8 +214,8 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
     for (int i = tid; i < kWarps * 256; i += kBlock) (&s_wh[0][0])[i] = 0u;
     __syncthreads();
     const uint32_t tile = s_tile;
-    const uint32_t base = tile * kSortTile;
-    const uint32_t tile_n = min(static_cast<uint32_t>(kSortTile), n - base);
+    const uint32_t base = tile * (kBlock * SI);
+    const uint32_t tile_n = min(static_cast<uint32_t>((kBlock * SI)), n - base);
 
     // digit tid over the whole input.  The first pass sums the histogram blocks'
     // counts (the first kHistPrefetch requested together with the tile's keys)
@@ -227,11 +229,11 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
     } else {
         hcount[0] = gh[tid];
     }
-    uint32_t key[kSortItems], val[kSortItems], rank[kSortItems];
-    int dig[kSortItems];
+    uint32_t key[SI], val[SI], rank[SI];
+    int dig[SI];
 #pragma unroll
-    for (int i = 0; i < kSortItems; ++i) {
-        const uint32_t local = warp * 32 * kSortItems + i * 32 + lane;
+    for (int i = 0; i < SI; ++i) {
+        const uint32_t local = warp * 32 * SI + i * 32 + lane;
         const bool valid = local < tile_n;
         uint32_t k = 0, v = 0;
         if (valid) {
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
     }
     const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
-    for (int i = 0; i < kSortItems; ++i) {
+    for (int i = 0; i < SI; ++i) {
         const int d = dig[i];
         const uint32_t peers = __match_any_sync(kFull, d);
         uint32_t b = 0;
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
     __syncthreads();
 
 #pragma unroll
-    for (int i = 0; i < kSortItems; ++i) {
+    for (int i = 0; i < SI; ++i) {
         const int d = dig[i];
         if (d < 256) {
             const uint32_t lp = s_texcl[d] + s_wh[warp][d] + rank[i];
@@ -370,6 +372,7 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
 //             one per list and warp; the order in which they are processed
 //             does not affect any result)
 // Status word of a tile: flag << 62 | heads << 31 | pieces.
+template <int RI>
 __global__ void __launch_bounds__(kBlock) k_run_detect(
     const uint32_t* __restrict__ skey, const uint32_t* __restrict__ sperm, uint32_t n,
     uint4* __restrict__ rec, uint32_t* __restrict__ seg_off, uint32_t* __restrict__ mlist,
@@ -393,30 +396,30 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     if (tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
     __syncthreads();
     const uint32_t tile = s_tile;
-    const uint32_t p0 = tile * kRunTile + tid * kRunItems;
+    const uint32_t p0 = tile * (kBlock * RI) + tid * RI;
 
-    uint32_t k[kRunItems];
+    uint32_t k[RI];
     uint32_t prev = 0;
     if (p0 < n && p0 > 0) prev = skey[p0 - 1];
-    if (p0 + kRunItems <= n) {
+    if (p0 + RI <= n) {
 #pragma unroll
-        for (int v4 = 0; v4 < kRunItems / 4; ++v4) {
+        for (int v4 = 0; v4 < RI / 4; ++v4) {
             const uint4 a = *reinterpret_cast<const uint4*>(skey + p0 + 4 * v4);
             k[4 * v4] = a.x; k[4 * v4 + 1] = a.y; k[4 * v4 + 2] = a.z; k[4 * v4 + 3] = a.w;
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kRunItems; ++i) k[i] = (p0 + i < n) ? skey[p0 + i] : 0u;
+        for (int i = 0; i < RI; ++i) k[i] = (p0 + i < n) ? skey[p0 + i] : 0u;
     }
     // a multiple q of kPieceLen inside a segment starts a new piece only when the
-    // segment already holds position q - kPieceLen (kRunItems divides kPieceLen:
+    // segment already holds position q - kPieceLen (RI divides kPieceLen:
     // at most the first item of a thread is such a multiple)
-    static_assert(kPieceLen % kRunItems == 0, "piece boundaries fall on a thread's first item");
+    static_assert(kPieceLen % RI == 0, "piece boundaries fall on a thread's first item");
     const bool at_boundary = (p0 < n) && (p0 % kPieceLen == 0) && p0 >= kPieceLen;
     const uint32_t key_back = at_boundary ? skey[p0 - kPieceLen] : 0u;
     uint32_t headm = 0, piecem = 0;
 #pragma unroll
-    for (int i = 0; i < kRunItems; ++i) {
+    for (int i = 0; i < RI; ++i) {
         const uint32_t q = p0 + i;
         if (q < n) {
             const uint32_t before = (i == 0) ? prev : k[i - 1];
@@ -429,21 +432,21 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     // everything the items below read is requested before the scan and the
     // look-back, whose round trips it then overlaps: input positions, the key at
     // the next piece boundary of each segment head, last_step
-    uint32_t pmv[kRunItems];
-    if (p0 + kRunItems <= n) {
+    uint32_t pmv[RI];
+    if (p0 + RI <= n) {
 #pragma unroll
-        for (int v4 = 0; v4 < kRunItems / 4; ++v4) {
+        for (int v4 = 0; v4 < RI / 4; ++v4) {
             const uint4 a = *reinterpret_cast<const uint4*>(sperm + p0 + 4 * v4);
             pmv[4 * v4] = a.x; pmv[4 * v4 + 1] = a.y; pmv[4 * v4 + 2] = a.z; pmv[4 * v4 + 3] = a.w;
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kRunItems; ++i) pmv[i] = (p0 + i < n) ? sperm[p0 + i] : 0u;
+        for (int i = 0; i < RI; ++i) pmv[i] = (p0 + i < n) ? sperm[p0 + i] : 0u;
     }
-    uint32_t nxt_key[kRunItems], long_key[kRunItems];
-    int64_t last[kRunItems];
+    uint32_t nxt_key[RI], long_key[RI];
+    int64_t last[RI];
 #pragma unroll
-    for (int i = 0; i < kRunItems; ++i) {
+    for (int i = 0; i < RI; ++i) {
         const uint32_t q = p0 + i;
         const bool h = (headm >> i) & 1u;
         // first boundary that can split a segment starting at q: the smallest
@@ -498,12 +501,12 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     uint32_t h_run = static_cast<uint32_t>(ex >> 31) + (xe >> 16);       // heads before p0
     uint32_t p_run = static_cast<uint32_t>(ex & 0x7fffffffull) + (xe & 0xffffu);
 
-    uint32_t lists[kRunItems];   // flagged pieces of this thread, in order
+    uint32_t lists[RI];   // flagged pieces of this thread, in order
     uint64_t kinds = 0;          // 3 bits per flagged piece: long, split head, group head
-    static_assert(3 * kRunItems <= 64, "kinds holds 3 bits per item");
+    static_assert(3 * RI <= 64, "kinds holds 3 bits per item");
     int nl = 0;
 #pragma unroll
-    for (int i = 0; i < kRunItems; ++i) {
+    for (int i = 0; i < RI; ++i) {
         const uint32_t q = p0 + i;
         if (q >= n) break;
         const bool h = (headm >> i) & 1u;
@@ -594,18 +597,20 @@ cudaError_t sort_and_segment(const int64_t* idx, int64_t n, int64_t c, int64_t b
         const int in = out ^ 1;
         uint32_t* st = ws.rstatus + static_cast<size_t>(p) * L.sort_tiles * 256;
         SO_PROFILE("radix_pass", s);
+        const bool large = L.sort_items != kSortItems;
+        const auto kern = p == 0 ? (large ? k_radix_pass<true, kSortItemsLarge> : k_radix_pass<true, kSortItems>)
+                                 : (large ? k_radix_pass<false, kSortItemsLarge> : k_radix_pass<false, kSortItems>);
         if (p == 0)
-            launch(k_radix_pass<true>, dim3(L.sort_tiles), dim3(kBlock), s, idx, nullptr, nullptr, ws.keys[out],
-                                                               ws.vals[out], nn, 8 * p, ws.bh, L.hist_blocks, ws.gh, L.passes, st,
-                                                               ws.counts + kCtrPass0 + p, d_err);
+            launch(kern, dim3(L.sort_tiles), dim3(kBlock), s, idx, nullptr, nullptr, ws.keys[out], ws.vals[out], nn,
+                   8 * p, ws.bh, L.hist_blocks, ws.gh, L.passes, st, ws.counts + kCtrPass0 + p, d_err);
         else
-            launch(k_radix_pass<false>, dim3(L.sort_tiles), dim3(kBlock), s, nullptr, ws.keys[in], ws.vals[in],
-                                                                ws.keys[out], ws.vals[out], nn, 8 * p,
-                                                                ws.bh, L.hist_blocks, ws.gh + 256 * p, L.passes, st,
-                                                                ws.counts + kCtrPass0 + p, d_err);
+            launch(kern, dim3(L.sort_tiles), dim3(kBlock), s, nullptr, ws.keys[in], ws.vals[in], ws.keys[out],
+                   ws.vals[out], nn, 8 * p, ws.bh, L.hist_blocks, ws.gh + 256 * p, L.passes, st,
+                   ws.counts + kCtrPass0 + p, d_err);
     }
     SO_PROFILE("run_detect", s);
-    launch(k_run_detect, dim3(L.run_tiles), dim3(kBlock), s, ws.keys[ws.final_buf], ws.vals[ws.final_buf], nn, ws.rec,
+    launch(L.run_items != kRunItems ? k_run_detect<kRunItemsLarge> : k_run_detect<kRunItems>, dim3(L.run_tiles),
+           dim3(kBlock), s, ws.keys[ws.final_buf], ws.vals[ws.final_buf], nn, ws.rec,
                                                 ws.seg_off, ws.mlist, ws.slist, ws.glist, ws.dstatus, ws.counts + kCtrRun, ws.counts,
                                                 idx_out, seg_off_out, perm_out, d_nnz_out, ls, ls_per_coord,
                                                 c, bound, t, d_err);

@@ -41,6 +41,8 @@ CANON_CASES = [
     (1500, 1000, 300, 200),
     (4096, 5, 1, 0),          # every entry the same key
     (70_000, 2, 100_000, 0),
+    (600_000, 1, 2_000_000, 3000),   # large-input tiles (16 keys per thread), 21-bit keys
+    (530_000, 4, 40_000_000, 0),     # large-input tiles, 26-bit keys (four passes)
 ]
 
 
