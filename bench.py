@@ -533,6 +533,9 @@ def run_workload(args):
             grads.append(so.row_coo(t2[0], t2[1], w.index_dist == "unique_sorted"))
     if any(h[0] == "coo" for h in host) and w.index_dist != "unique_sorted":
         ws = so.workspace(w.lookups, c, w.rows, dev)
+    elif any(h[0] == "csr" for h in host) and w.index_dist != "csr_elem":
+        # full-row CSR with a per-row last_step: room for the list of listed rows (<= lookups)
+        ws = so.workspace(w.lookups + 1, 1, w.rows, dev)
     acfg = so.AdamConfig(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps)
     scfg = so.SgdConfig(lr=w.lr, momentum=w.momentum, weight_decay=w.weight_decay)
     amode = so.DORMANCY_DECAY if dd else so.LAZY

@@ -60,6 +60,11 @@
  *             256-byte aligned; its contents need not be initialised and are
  *             garbage after the call; calls that run concurrently need separate
  *             workspaces.  Canonical and CSR gradients need none (ws may be NULL).
+ *             A CSR Adam step with a per-row last_step (every listed row full)
+ *             given ws of at least 8*(nnz/c + 1) bytes (256-byte aligned;
+ *             sparse_workspace_size(nnz/c + 1, 1, r) is enough) lists the touched
+ *             rows there and updates them with the row kernel, which spreads them
+ *             evenly over the GPU; without it the CSR kernel walks the rows.
  *   Step.     t is the global step, the 1-based number of step calls so far; it
  *             is owned by the caller and is the same t for every coordinate.
  *   State.    m, v, buf start at 0 and last_step at 0 (never touched).  A

@@ -169,7 +169,7 @@ sparse_status_t sparse_csr_to_coo(const int64_t* row_off, const int32_t* cols, i
         return SPARSE_ERR_INVALID_ARG;
     if (r > 0 && c > INT64_MAX / r) return SPARSE_ERR_INVALID_ARG;
     if (nnz > 0 && (cols == nullptr || lin_out == nullptr)) return SPARSE_ERR_INVALID_ARG;
-    cudaError_t e = csr_check(row_off, cols, r, c, nnz, 0, nullptr, 0, 0, d_err, stream);
+    cudaError_t e = csr_check(row_off, cols, r, c, nnz, 0, nullptr, 0, 0, nullptr, d_err, stream);
     if (e == cudaSuccess && nnz > 0) e = csr_to_coo(row_off, cols, r, c, nnz, lin_out, d_err, stream);
     return from_cuda(e);
 }
@@ -215,8 +215,22 @@ sparse_status_t sparse_adam_table_step(float* p, float* m, float* v, int64_t* la
     cudaError_t e = cudaSuccess;
 
     if (grad->form == SPARSE_GRAD_CSR) {
-        e = csr_check(grad->row_off, grad->cols, r, c, n, !per_coord, last_step, per_coord, t, d_err, stream);
-        if (e == cudaSuccess && n > 0) e = csr_adam(grad->row_off, grad->cols, grad->vals, r, c, n, P, d_err, stream);
+        // Per-row last_step: every listed row is full, so with scratch for the list of
+        // listed rows (filled by the check) the gradient is a canonical row-COO over the
+        // CSR's own values and takes the row kernel; otherwise the CSR kernel.
+        const int64_t nrows = n / c;
+        const bool as_rows = !per_coord && n > 0 && ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0 &&
+                             ws_bytes >= sizeof(int64_t) * static_cast<size_t>(nrows + 1) && nrows <= kMaxCanonN &&
+                             r <= kMaxRawBound;
+        int64_t* rows_list = as_rows ? static_cast<int64_t*>(ws) : nullptr;
+        e = csr_check(grad->row_off, grad->cols, r, c, n, !per_coord, last_step, per_coord, t, rows_list, d_err,
+                      stream);
+        if (e == cudaSuccess && as_rows) {
+            const int vec4 = (c % 4 == 0) && aligned16(p) && aligned16(m) && aligned16(v) && aligned16(grad->vals);
+            e = fused_rows_adam_canon(rows_list, nrows, grad->vals, c, P, vec4, d_err, stream);
+        } else if (e == cudaSuccess && n > 0) {
+            e = csr_adam(grad->row_off, grad->cols, grad->vals, r, c, n, P, d_err, stream);
+        }
         return from_cuda(e);
     }
     if (n == 0) return SPARSE_OK;
@@ -263,7 +277,7 @@ sparse_status_t sparse_sgd_table_step(float* p, float* buf, int64_t r, int64_t c
     const int64_t n = grad->n;
     cudaError_t e = cudaSuccess;
     if (grad->form == SPARSE_GRAD_CSR) {
-        e = csr_check(grad->row_off, grad->cols, r, c, n, 0, nullptr, 0, 0, d_err, stream);
+        e = csr_check(grad->row_off, grad->cols, r, c, n, 0, nullptr, 0, 0, nullptr, d_err, stream);
         if (e == cudaSuccess && n > 0) e = csr_sgd(grad->row_off, grad->cols, grad->vals, r, c, n, P, d_err, stream);
         return from_cuda(e);
     }
@@ -311,7 +325,7 @@ sparse_status_t sparse_check_state(const float* m, const float* v, int64_t r, in
     if (d_err == nullptr || (r > 0 && (m == nullptr || v == nullptr))) return SPARSE_ERR_INVALID_ARG;
     const int64_t n = grad->n;
     if (grad->form == SPARSE_GRAD_CSR) {
-        cudaError_t e = csr_check(grad->row_off, grad->cols, r, c, n, 0, nullptr, 0, 0, d_err, stream);
+        cudaError_t e = csr_check(grad->row_off, grad->cols, r, c, n, 0, nullptr, 0, 0, nullptr, d_err, stream);
         if (e == cudaSuccess && n > 0) e = check_state_csr(grad->row_off, grad->cols, r, c, n, m, v, d_err, stream);
         return from_cuda(e);
     }

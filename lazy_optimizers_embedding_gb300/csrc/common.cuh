@@ -314,9 +314,10 @@ cudaError_t fused_rows_store_sorted(const SortWs& ws, const WsLayout& L, const f
                                     const StoreParams& P, int vec4, int32_t* d_err, cudaStream_t s);
 
 // CSR (element-granular) paths.
+// rows_list (full_rows only, may be NULL): filled with the listed rows, see k_csr_check.
 cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, int64_t c, int64_t nnz,
-                      int full_rows, const int64_t* ls, int ls_per_coord, int64_t t, int32_t* d_err,
-                      cudaStream_t s);
+                      int full_rows, const int64_t* ls, int ls_per_coord, int64_t t, int64_t* rows_list,
+                      int32_t* d_err, cudaStream_t s);
 cudaError_t read_rows(const float* table, int64_t r, int64_t c, const int64_t* idx, int64_t n, float* out, int vec4,
                       int32_t* d_err, cudaStream_t s);
 cudaError_t check_finite(const float* vals, int64_t n, int32_t* d_err, cudaStream_t s);

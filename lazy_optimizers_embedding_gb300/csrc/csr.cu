@@ -103,12 +103,17 @@ __device__ __forceinline__ unsigned full_row_mask(const Group& G, int64_t r0, in
 __device__ __forceinline__ int nth_row(unsigned mask, int k) { return static_cast<int>(__fns(mask, 0, k + 1)); }
 
 // Validation of a CSR gradient (and of last_step < t on its touched coordinates).
+// With rows_list (only when every listed row must be full): the j-th listed row,
+// whose entries start at offset j*c, is recorded as rows_list[j], so that the
+// list with the CSR's value array is the same gradient as a canonical row-COO.
+// Offsets are validated before any slot is written, so a malformed CSR (which
+// sets *d_err) never writes outside rows_list[0 .. nnz/c).
 template <int TQ>
 __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict__ row_off,
                                                       const int32_t* __restrict__ cols, int64_t r,
                                                       int64_t c, int64_t nnz, int full_rows,
                                                       const int64_t* __restrict__ ls, int ls_per_coord,
-                                                      int64_t t, int32_t* d_err)
+                                                      int64_t t, int64_t* __restrict__ rows_list, int32_t* d_err)
 {
     pdl_enter();
     const int lane = threadIdx.x & 31;
@@ -130,8 +135,10 @@ __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict_
         const int64_t rr = r0 + lane;
         if (rr < r && G.b > G.a) {
             if (full_rows && G.b - G.a != c) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
+            else if (rows_list && G.a % c == 0) rows_list[G.a / c] = rr;
             if (ls && !ls_per_coord && ls[rr] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
         }
+        if (full_rows) continue;   // columns checked below, entry by entry
         const unsigned fullmask = full_row_mask<TQ>(G, r0, r, c);
         if constexpr (TQ > 0) {
             // a listed full row is canonical iff its columns are exactly 0 .. c-1
@@ -197,6 +204,16 @@ __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict_
                 if (prev[u] >= col[u]) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
                 if (ls && ls_per_coord && ls[(r0 + l[u]) * c + col[u]] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
             }
+        }
+    }
+    if (full_rows) {
+        // Every listed row must hold all c columns, so (the offsets being multiples of
+        // c) entry j must be column j % c: one flat pass over the column array.
+        const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
+        for (int64_t j = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; j < nnz; j += stride) {
+            const int32_t col = cols[j];
+            if (col != j % c) set_error(d_err, (col < 0 || col >= c) ? SPARSE_ERR_INDEX_OUT_OF_RANGE
+                                                                    : SPARSE_ERR_NOT_CANONICAL);
         }
     }
 }
@@ -368,11 +385,19 @@ struct CsrSgdOp {
 // Blocks of the CSR kernels: one warp per group of 32 rows, at most
 // SO_CSR_BLOCKS_PER_SM blocks per SM (several waves: a block that finds only
 // empty groups retires quickly and its slot takes the next block).
-static int group_blocks(int64_t r)
+// The check kernel's cap; with full rows (offsets, last_step and a flat column
+// pass only) fewer blocks, each walking more groups, measured faster.
+#ifndef SO_CSR_CHECK_BLOCKS_PER_SM
+#define SO_CSR_CHECK_BLOCKS_PER_SM SO_CSR_BLOCKS_PER_SM
+#endif
+#ifndef SO_CSR_CHECK_FULL_BLOCKS_PER_SM
+#define SO_CSR_CHECK_FULL_BLOCKS_PER_SM 4
+#endif
+static int group_blocks(int64_t r, int per_sm = SO_CSR_BLOCKS_PER_SM)
 {
     const int64_t groups = (r + 31) / 32;
     const int64_t want = (groups + kBlock / 32 - 1) / (kBlock / 32);
-    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(SO_CSR_BLOCKS_PER_SM) * num_sms())));
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(per_sm) * num_sms())));
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -398,14 +423,17 @@ static int full_row_team(int64_t c, bool aligned)
     }
 
 cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, int64_t c, int64_t nnz,
-                      int full_rows, const int64_t* ls, int ls_per_coord, int64_t t, int32_t* d_err,
-                      cudaStream_t s)
+                      int full_rows, const int64_t* ls, int ls_per_coord, int64_t t, int64_t* rows_list,
+                      int32_t* d_err, cudaStream_t s)
 {
     SO_PROFILE("csr_check", s);
     const int tq = full_row_team(c, aligned16(cols));
 #define SO_CHECK(T)                                                                                              \
-    launch(k_csr_check<T>, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, r, c, nnz, full_rows, ls,        \
-           ls_per_coord, t, d_err)
+    launch(k_csr_check<T>,                                                                                      \
+           dim3(group_blocks(r, full_rows ? SO_CSR_CHECK_FULL_BLOCKS_PER_SM : SO_CSR_CHECK_BLOCKS_PER_SM)),     \
+           dim3(kBlock), s, row_off, cols, r, c,                                                                 \
+           nnz, full_rows, ls,                                                                                      \
+           ls_per_coord, t, full_rows ? rows_list : nullptr, d_err)
     SO_TQ_DISPATCH(tq, SO_CHECK)
 #undef SO_CHECK
     return cudaGetLastError();

@@ -242,6 +242,8 @@ def test_csr_adam_fullsize(cuda_lib, cfg):
     m[sel], v[sel] = dev(m0), dev(v0)
     ls = G.zeros(w.rows * w.cols if per_coord else w.rows, torch.int64)
     err = G.error_word()
+    # the full-row workload gets the workspace the benchmark passes (its rows then take the row kernel)
+    ws = None if per_coord else G.workspace(so, w.lookups + 1, 1, w.rows)
     cfgc = so.AdamConfig(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps)
     ohp = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps)
     layout = so.LAST_STEP_PER_COORD if per_coord else so.LAST_STEP_PER_ROW
@@ -254,7 +256,7 @@ def test_csr_adam_fullsize(cuda_lib, cfg):
     for t, (ro, co, va) in enumerate(_stream(make, w.steps), start=1):
         g = so.csr(dev(ro), dev(co), dev(va))
         so.check(so.sparse_adam_table_step(p, m, v, ls, layout, w.rows, w.cols, g, t, cfgc, so.DORMANCY_DECAY,
-                                           None, err), "csr step")
+                                           ws, err), "csr step")
         so_off, so_cols, so_vals = _csr_rows_subset(ro, co, va, rows)
         for i in range(rows.shape[0]):
             tmask[i, so_cols[so_off[i]:so_off[i + 1]]] = True

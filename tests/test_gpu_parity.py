@@ -117,12 +117,13 @@ def _test_key():
     return os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0].split("::")[-1]
 
 
-def _run_adam(so, R, c, steps, mode, gen, form, layout=None, hp=ADAM, check_every=False):
+def _run_adam(so, R, c, steps, mode, gen, form, layout=None, hp=ADAM, check_every=False, csr_ws=False):
     """gen(step) -> gradient for the step, in the given form; runs GPU and oracle side by side.
 
     Every device array is guarded (canaries checked after each step); coordinates that no step
     touches hold planted specials in p, m, v (and large or negative values in last_step) and
-    must come back bit for bit; touched m and v are held to the no-floor checks of gpu_harness."""
+    must come back bit for bit; touched m and v are held to the no-floor checks of gpu_harness.
+    csr_ws: CSR steps get a workspace (full rows with a per-row last_step then take the row path)."""
     import torch
     key = _test_key()
     rng = np.random.default_rng(R + c)
@@ -156,6 +157,8 @@ def _run_adam(so, R, c, steps, mode, gen, form, layout=None, hp=ADAM, check_ever
     scale = MomentScale((R, c), ls_n, ohp, omode, per_coord)
     touched = np.zeros((R, c), bool)
     ws = None
+    if form == "csr" and csr_ws:
+        ws = G.workspace(so, max(g[1].shape[0] for g in grads) // c + 1, 1, R)
     for s in range(steps):
         t = s + 1
         g = grads[s]
@@ -174,7 +177,7 @@ def _run_adam(so, R, c, steps, mode, gen, form, layout=None, hp=ADAM, check_ever
         else:
             row_off, cols, vals = g
             grad = so.csr(G.array(row_off), G.array(cols), G.array(vals))
-            so.check(so.sparse_adam_table_step(p, m, v, ls, layout, R, c, grad, t, cfg, mode, None, err),
+            so.check(so.sparse_adam_table_step(p, m, v, ls, layout, R, c, grad, t, cfg, mode, ws, err),
                      "adam_table_step csr")
             rc = oracle.adam_table_step(op, om, ov, ols, t, row_off=row_off, cols=cols, vals=vals, mode=omode,
                                         ls_per_coord=per_coord, **ohp)
@@ -255,9 +258,11 @@ def test_adam_csr_element_granular(cuda_lib, mode, R, c, nrows, k):
               layout=so.LAST_STEP_PER_COORD, check_every=True)
 
 
+@pytest.mark.parametrize("csr_ws", [False, True], ids=["csr_kernel", "row_path"])
 @pytest.mark.parametrize("mode", [0, 1], ids=["lazy", "dormancy_decay"])
-def test_adam_csr_full_rows_per_row_last_step(cuda_lib, mode):
-    """A CSR whose listed rows are full, with one last_step per row (the summed-lookups shape)."""
+def test_adam_csr_full_rows_per_row_last_step(cuda_lib, mode, csr_ws):
+    """A CSR whose listed rows are full, with one last_step per row (the summed-lookups shape), through the
+    CSR kernel (no workspace) and through the row kernel over the compacted rows (workspace given)."""
     so = cuda_lib
     R, c = 3000, 64
 
@@ -267,7 +272,7 @@ def test_adam_csr_full_rows_per_row_last_step(cuda_lib, mode):
         ro, co = oracle.row_coo_to_csr(rows, R, c)
         return ro, co, rng.standard_normal(rows.shape[0] * c).astype(np.float32)
 
-    _run_adam(so, R, c, 5, mode, gen, "csr", layout=so.LAST_STEP_PER_ROW, check_every=True)
+    _run_adam(so, R, c, 5, mode, gen, "csr", layout=so.LAST_STEP_PER_ROW, check_every=True, csr_ws=csr_ws)
 
 
 @pytest.mark.parametrize("wd_mode", [0, 1], ids=["l2", "decoupled"])
@@ -295,7 +300,7 @@ def test_adam_weight_decay(cuda_lib, wd_mode, mode, form):
 
     f = "csr" if form.startswith("csr") else form
     layout = so.LAST_STEP_PER_COORD if form == "csr_elem" else so.LAST_STEP_PER_ROW
-    _run_adam(so, R, c, 4, mode, gen, f, layout=layout, hp=hp, check_every=True)
+    _run_adam(so, R, c, 4, mode, gen, f, layout=layout, hp=hp, check_every=True, csr_ws=(form == "csr_full"))
 
 
 def test_adam_weight_decay_bad_settings_rejected(cuda_lib):
