@@ -127,7 +127,7 @@ def hbm_peak():
     return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "launches_table_10Mx128_zipf1.05_adam_dd.md")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "row_kernel_traffic.json")
 ROW_KERNEL_SOURCES = ("fused.cuh", "common.cuh", "fused_adam.cu")
 
 
@@ -139,15 +139,13 @@ def row_kernel_digest():
 
 
 def recorded_traffic():
-    """DRAM bytes (read + write) per launch of the row kernel from the committed ncu capture of
-    this workload, or None once the kernel sources differ from the captured ones."""
+    """DRAM bytes (read + write) per launch of the row kernel from the committed ncu record
+    (profiles/row_kernel_traffic.json), or None once the kernel sources differ from the captured ones."""
     try:
-        with open(PROFILE_SUMMARY) as f:
-            fields = dict(line.split(": ", 1) for line in f.read().splitlines()
-                          if line.startswith(("traffic_bytes_per_launch: ", "kernel_source_digest: ")))
-        if fields.get("kernel_source_digest", "").strip() != row_kernel_digest():
+        rec = json.load(open(TRAFFIC_RECORD))
+        if rec.get("kernel_source_digest") != row_kernel_digest():
             return None
-        return int(fields["traffic_bytes_per_launch"])
+        return int(rec["traffic_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
 
@@ -414,7 +412,8 @@ def run_ours(args):
                          "frac": (achieved / peak) if achieved else None,
                          "traffic": recorded_traffic() if (w is wl.CFG_ZIPF_10M_128 and dd) else None,
                          "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
-                                           "committed launch-list summary (null once the kernel sources change)",
+                                           "profiles/row_kernel_traffic.json (a 2M-row capture scaled to the "
+                                           "full launch; null once the kernel sources change)",
                          "peak_source": peak_src, "bytes_per_launch": dom_bytes,
                          "avg_launch_us": dom_avg_s * 1e6},
             "kernel_share": {k: {"launches": l, "ms": ms, "share": ms / total_prof if total_prof else None}
