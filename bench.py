@@ -535,6 +535,9 @@ def run_workload(args):
     elif any(h[0] == "csr" for h in host) and w.index_dist != "csr_elem":
         # full-row CSR with a per-row last_step: room for the list of listed rows (<= lookups)
         ws = so.workspace(w.lookups + 1, 1, w.rows, dev)
+    elif any(h[0] == "csr" for h in host):
+        # element CSR with a per-coordinate last_step: room for every entry's row and gap
+        ws = so.workspace(max(int(h[2].shape[0]) for h in host) + 64, 1, w.rows, dev)
     acfg = so.AdamConfig(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps)
     scfg = so.SgdConfig(lr=w.lr, momentum=w.momentum, weight_decay=w.weight_decay)
     amode = so.DORMANCY_DECAY if dd else so.LAZY

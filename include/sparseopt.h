@@ -64,7 +64,13 @@
  *             given ws of at least 8*(nnz/c + 1) bytes (256-byte aligned;
  *             sparse_workspace_size(nnz/c + 1, 1, r) is enough) lists the touched
  *             rows there and updates them with the row kernel, which spreads them
- *             evenly over the GPU; without it the CSR kernel walks the rows.
+ *             evenly over the GPU; without it the CSR kernel walks the rows.  Any
+ *             other CSR step (per-coordinate last_step, or SGD) given ws of at
+ *             least 8*(nnz + 64) bytes for Adam or 4*(nnz + 64) for SGD (256-byte
+ *             aligned, rows < 2^31, t < 2^31; sparse_workspace_size(nnz + 64, 1, r)
+ *             is enough) records every entry's row (and last_step gap) there during
+ *             the check and updates one entry per thread without re-reading
+ *             last_step.
  *   Step.     t is the global step, the 1-based number of step calls so far; it
  *             is owned by the caller and is the same t for every coordinate.
  *   State.    m, v, buf start at 0 and last_step at 0 (never touched).  A

@@ -84,6 +84,15 @@ sparse_status_t check_ws(int64_t n, int64_t c, int64_t bound, void* ws, size_t w
     return SPARSE_OK;
 }
 
+// Per-entry scratch of the flat CSR update: `arrays` int32 arrays of nnz entries,
+// each starting 256-byte aligned; rows must fit int32.
+int64_t flat_stride(int64_t nnz) { return (nnz + 63) / 64 * 64; }
+bool flat_fits(const void* ws, size_t ws_bytes, int64_t nnz, int64_t r, int arrays)
+{
+    return ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0 && r <= INT32_MAX &&
+           ws_bytes >= sizeof(int32_t) * static_cast<size_t>(flat_stride(nnz)) * static_cast<size_t>(arrays);
+}
+
 // Common validation of a gradient descriptor against an (r, c) table.
 sparse_status_t check_grad(const sparse_grad_t* g, int64_t r, int64_t c)
 {
@@ -169,7 +178,7 @@ sparse_status_t sparse_csr_to_coo(const int64_t* row_off, const int32_t* cols, i
         return SPARSE_ERR_INVALID_ARG;
     if (r > 0 && c > INT64_MAX / r) return SPARSE_ERR_INVALID_ARG;
     if (nnz > 0 && (cols == nullptr || lin_out == nullptr)) return SPARSE_ERR_INVALID_ARG;
-    cudaError_t e = csr_check(row_off, cols, r, c, nnz, 0, nullptr, 0, 0, nullptr, d_err, stream);
+    cudaError_t e = csr_check(row_off, cols, r, c, nnz, 0, nullptr, 0, 0, nullptr, nullptr, nullptr, d_err, stream);
     if (e == cudaSuccess && nnz > 0) e = csr_to_coo(row_off, cols, r, c, nnz, lin_out, d_err, stream);
     return from_cuda(e);
 }
@@ -223,11 +232,20 @@ sparse_status_t sparse_adam_table_step(float* p, float* m, float* v, int64_t* la
                              ws_bytes >= sizeof(int64_t) * static_cast<size_t>(nrows + 1) && nrows <= kMaxCanonN &&
                              r <= kMaxRawBound;
         int64_t* rows_list = as_rows ? static_cast<int64_t*>(ws) : nullptr;
-        e = csr_check(grad->row_off, grad->cols, r, c, n, !per_coord, last_step, per_coord, t, rows_list, d_err,
-                      stream);
+        // Per-coordinate last_step: with scratch for every entry's row and gap (filled by
+        // the check), the update is one entry per thread and does not read last_step.
+        int32_t *ent_row = nullptr, *ent_gap = nullptr;
+        if (per_coord && n > 0 && t <= INT32_MAX && flat_fits(ws, ws_bytes, n, r, 2)) {
+            ent_row = static_cast<int32_t*>(ws);
+            ent_gap = ent_row + flat_stride(n);
+        }
+        e = csr_check(grad->row_off, grad->cols, r, c, n, !per_coord, last_step, per_coord, t, rows_list, ent_row,
+                      ent_gap, d_err, stream);
         if (e == cudaSuccess && as_rows) {
             const int vec4 = (c % 4 == 0) && aligned16(p) && aligned16(m) && aligned16(v) && aligned16(grad->vals);
             e = fused_rows_adam_canon(rows_list, nrows, grad->vals, c, P, vec4, d_err, stream);
+        } else if (e == cudaSuccess && ent_row) {
+            e = csr_adam_flat(grad->cols, grad->vals, ent_row, ent_gap, c, n, P, d_err, stream);
         } else if (e == cudaSuccess && n > 0) {
             e = csr_adam(grad->row_off, grad->cols, grad->vals, r, c, n, P, d_err, stream);
         }
@@ -277,8 +295,13 @@ sparse_status_t sparse_sgd_table_step(float* p, float* buf, int64_t r, int64_t c
     const int64_t n = grad->n;
     cudaError_t e = cudaSuccess;
     if (grad->form == SPARSE_GRAD_CSR) {
-        e = csr_check(grad->row_off, grad->cols, r, c, n, 0, nullptr, 0, 0, nullptr, d_err, stream);
-        if (e == cudaSuccess && n > 0) e = csr_sgd(grad->row_off, grad->cols, grad->vals, r, c, n, P, d_err, stream);
+        // with scratch for every entry's row (filled by the check), one entry per thread
+        int32_t* ent_row = (n > 0 && flat_fits(ws, ws_bytes, n, r, 1)) ? static_cast<int32_t*>(ws) : nullptr;
+        e = csr_check(grad->row_off, grad->cols, r, c, n, 0, nullptr, 0, 0, nullptr, ent_row, nullptr, d_err, stream);
+        if (e == cudaSuccess && ent_row)
+            e = csr_sgd_flat(grad->cols, grad->vals, ent_row, c, n, P, d_err, stream);
+        else if (e == cudaSuccess && n > 0)
+            e = csr_sgd(grad->row_off, grad->cols, grad->vals, r, c, n, P, d_err, stream);
         return from_cuda(e);
     }
     if (n == 0) return SPARSE_OK;
@@ -325,7 +348,7 @@ sparse_status_t sparse_check_state(const float* m, const float* v, int64_t r, in
     if (d_err == nullptr || (r > 0 && (m == nullptr || v == nullptr))) return SPARSE_ERR_INVALID_ARG;
     const int64_t n = grad->n;
     if (grad->form == SPARSE_GRAD_CSR) {
-        cudaError_t e = csr_check(grad->row_off, grad->cols, r, c, n, 0, nullptr, 0, 0, nullptr, d_err, stream);
+        cudaError_t e = csr_check(grad->row_off, grad->cols, r, c, n, 0, nullptr, 0, 0, nullptr, nullptr, nullptr, d_err, stream);
         if (e == cudaSuccess && n > 0) e = check_state_csr(grad->row_off, grad->cols, r, c, n, m, v, d_err, stream);
         return from_cuda(e);
     }

@@ -314,10 +314,16 @@ cudaError_t fused_rows_store_sorted(const SortWs& ws, const WsLayout& L, const f
                                     const StoreParams& P, int vec4, int32_t* d_err, cudaStream_t s);
 
 // CSR (element-granular) paths.
-// rows_list (full_rows only, may be NULL): filled with the listed rows, see k_csr_check.
+// rows_list (full_rows only, may be NULL): filled with the listed rows; ent_row /
+// ent_gap (not full_rows, may be NULL): every entry's row and gap; see k_csr_check.
 cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, int64_t c, int64_t nnz,
                       int full_rows, const int64_t* ls, int ls_per_coord, int64_t t, int64_t* rows_list,
-                      int32_t* d_err, cudaStream_t s);
+                      int32_t* ent_row, int32_t* ent_gap, int32_t* d_err, cudaStream_t s);
+// Element-granular CSR updates from the check's per-entry rows (and gaps).
+cudaError_t csr_adam_flat(const int32_t* cols, const float* vals, const int32_t* ent_row, const int32_t* ent_gap,
+                          int64_t c, int64_t nnz, const AdamParams& P, int32_t* d_err, cudaStream_t s);
+cudaError_t csr_sgd_flat(const int32_t* cols, const float* vals, const int32_t* ent_row, int64_t c, int64_t nnz,
+                         const SgdParams& P, int32_t* d_err, cudaStream_t s);
 cudaError_t read_rows(const float* table, int64_t r, int64_t c, const int64_t* idx, int64_t n, float* out, int vec4,
                       int32_t* d_err, cudaStream_t s);
 cudaError_t check_finite(const float* vals, int64_t n, int32_t* d_err, cudaStream_t s);

@@ -108,13 +108,21 @@ __device__ __forceinline__ int nth_row(unsigned mask, int k) { return static_cas
 // list with the CSR's value array is the same gradient as a canonical row-COO.
 // Offsets are validated before any slot is written, so a malformed CSR (which
 // sets *d_err) never writes outside rows_list[0 .. nnz/c).
+// With ent_row (rows not required full): every entry's row, and with ent_gap its
+// t - last_step (per-coordinate last_step; at most INT32_MAX), for the flat update.
 template <int TQ>
 __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict__ row_off,
                                                       const int32_t* __restrict__ cols, int64_t r,
                                                       int64_t c, int64_t nnz, int full_rows,
                                                       const int64_t* __restrict__ ls, int ls_per_coord,
-                                                      int64_t t, int64_t* __restrict__ rows_list, int32_t* d_err)
+                                                      int64_t t, int64_t* __restrict__ rows_list,
+                                                      int32_t* __restrict__ ent_row, int32_t* __restrict__ ent_gap,
+                                                      int32_t* d_err)
 {
+    const auto gap_of = [t](int64_t last) {
+        const int64_t gap = t - last;
+        return static_cast<int32_t>(gap < INT32_MAX ? gap : INT32_MAX);
+    };
     pdl_enter();
     const int lane = threadIdx.x & 31;
     if (blockIdx.x == 0 && threadIdx.x == 0 && (row_off[0] != 0 || row_off[r] != nnz))
@@ -167,10 +175,17 @@ __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict_
                                          cc[u].z < 0 || cc[u].z >= c || cc[u].w < 0 || cc[u].w >= c;
                         set_error(d_err, out ? SPARSE_ERR_INDEX_OUT_OF_RANGE : SPARSE_ERR_NOT_CANONICAL);
                     }
+                    const int64_t a = __shfl_sync(kFull, G.a, lr[u]) + 4 * q;   // this lane's four entries
                     if (ls && ls_per_coord) {
                         const int64_t i = (r0 + lr[u]) * c + 4 * q;
-                        for (int e = 0; e < 4; ++e)
-                            if (ls[i + e] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                        for (int e = 0; e < 4; ++e) {
+                            const int64_t last = ls[i + e];
+                            if (last >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                            if (ent_gap) ent_gap[a + e] = gap_of(last);
+                        }
+                    }
+                    if (ent_row) {
+                        for (int e = 0; e < 4; ++e) ent_row[a + e] = static_cast<int32_t>(r0 + lr[u]);
                     }
                 }
             }
@@ -202,7 +217,12 @@ __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict_
                     continue;
                 }
                 if (prev[u] >= col[u]) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
-                if (ls && ls_per_coord && ls[(r0 + l[u]) * c + col[u]] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                if (ls && ls_per_coord) {
+                    const int64_t last = ls[(r0 + l[u]) * c + col[u]];
+                    if (last >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                    if (ent_gap) ent_gap[j[u]] = gap_of(last);
+                }
+                if (ent_row) ent_row[j[u]] = static_cast<int32_t>(r0 + l[u]);
             }
         }
     }
@@ -424,7 +444,7 @@ static int full_row_team(int64_t c, bool aligned)
 
 cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, int64_t c, int64_t nnz,
                       int full_rows, const int64_t* ls, int ls_per_coord, int64_t t, int64_t* rows_list,
-                      int32_t* d_err, cudaStream_t s)
+                      int32_t* ent_row, int32_t* ent_gap, int32_t* d_err, cudaStream_t s)
 {
     SO_PROFILE("csr_check", s);
     const int tq = full_row_team(c, aligned16(cols));
@@ -433,7 +453,8 @@ cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, in
            dim3(group_blocks(r, full_rows ? SO_CSR_CHECK_FULL_BLOCKS_PER_SM : SO_CSR_CHECK_BLOCKS_PER_SM)),     \
            dim3(kBlock), s, row_off, cols, r, c,                                                                 \
            nnz, full_rows, ls,                                                                                      \
-           ls_per_coord, t, full_rows ? rows_list : nullptr, d_err)
+           ls_per_coord, t, full_rows ? rows_list : nullptr, full_rows ? nullptr : ent_row,                     \
+           full_rows ? nullptr : ent_gap, d_err)
     SO_TQ_DISPATCH(tq, SO_CHECK)
 #undef SO_CHECK
     return cudaGetLastError();
@@ -507,6 +528,101 @@ cudaError_t check_state_csr(const int64_t* row_off, const int32_t* cols, int64_t
 {
     SO_PROFILE("check_state_csr", s);
     launch(k_check_state_csr, dim3(group_blocks(r)), dim3(kBlock), s, row_off, cols, r, c, nnz, m, v, d_err);
+    return cudaGetLastError();
+}
+
+// Element-granular update from the check's per-entry rows (and gaps): one entry
+// per thread, kFlatIlp entries requested at once, no walk over the rows and no
+// read of last_step (the check read it; it is only rewritten here).
+constexpr int kFlatIlp = 4;
+
+struct FlatAdamOp {
+    AdamParams P;
+    __device__ __forceinline__ void apply(int64_t off, int32_t gap, float g, float& p, float& m, float& v) const
+    {
+        float b1 = P.beta1, b2 = P.beta2;
+        if (P.dd) dormancy_factors(P, gap, b1, b2);
+        adam_coord(P, b1, b2, g, p, m, v);
+        P.p[off] = p;
+        P.m[off] = m;
+        P.v[off] = v;
+        P.ls[off] = P.t;
+    }
+    __device__ __forceinline__ void load(int64_t off, float& p, float& m, float& v) const
+    {
+        p = P.p[off];
+        m = P.m[off];
+        v = P.v[off];
+    }
+};
+
+struct FlatSgdOp {
+    SgdParams P;
+    __device__ __forceinline__ void apply(int64_t off, int32_t, float g, float& p, float& b, float&) const
+    {
+        sgd_coord(P, g, p, b);
+        P.p[off] = p;
+        if (P.buf) P.buf[off] = b;
+    }
+    __device__ __forceinline__ void load(int64_t off, float& p, float& b, float&) const
+    {
+        p = P.p[off];
+        b = P.buf ? P.buf[off] : 0.0f;
+    }
+};
+
+template <class Op>
+__global__ void __launch_bounds__(kBlock) k_csr_flat(const int32_t* __restrict__ cols, const float* __restrict__ vals,
+                                                     const int32_t* __restrict__ ent_row,
+                                                     const int32_t* __restrict__ ent_gap, int64_t c, int64_t nnz,
+                                                     Op op, int32_t* d_err)
+{
+    pdl_enter();
+    if (read_error(d_err)) return;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
+    for (int64_t j0 = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; j0 < nnz; j0 += stride * kFlatIlp) {
+        int64_t off[kFlatIlp];
+        int32_t gap[kFlatIlp];
+        float g[kFlatIlp], x0[kFlatIlp], x1[kFlatIlp], x2[kFlatIlp];
+#pragma unroll
+        for (int u = 0; u < kFlatIlp; ++u) {
+            const int64_t j = j0 + u * stride;
+            if (j < nnz) {
+                off[u] = static_cast<int64_t>(__ldcs(ent_row + j)) * c + __ldcs(cols + j);
+                g[u] = __ldcs(vals + j);
+                gap[u] = ent_gap ? __ldcs(ent_gap + j) : 1;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kFlatIlp; ++u)
+            if (j0 + u * stride < nnz) op.load(off[u], x0[u], x1[u], x2[u]);
+#pragma unroll
+        for (int u = 0; u < kFlatIlp; ++u)
+            if (j0 + u * stride < nnz) op.apply(off[u], gap[u], g[u], x0[u], x1[u], x2[u]);
+    }
+}
+
+static int flat_grid(int64_t nnz)
+{
+    const int64_t want = (nnz + static_cast<int64_t>(kBlock) * kFlatIlp - 1) / (static_cast<int64_t>(kBlock) * kFlatIlp);
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 8 * num_sms())));
+}
+
+cudaError_t csr_adam_flat(const int32_t* cols, const float* vals, const int32_t* ent_row, const int32_t* ent_gap,
+                          int64_t c, int64_t nnz, const AdamParams& P, int32_t* d_err, cudaStream_t s)
+{
+    SO_PROFILE("csr_flat_adam", s);
+    launch(k_csr_flat<FlatAdamOp>, dim3(flat_grid(nnz)), dim3(kBlock), s, cols, vals, ent_row, P.dd ? ent_gap : nullptr,
+           c, nnz, FlatAdamOp{P}, d_err);
+    return cudaGetLastError();
+}
+
+cudaError_t csr_sgd_flat(const int32_t* cols, const float* vals, const int32_t* ent_row, int64_t c, int64_t nnz,
+                         const SgdParams& P, int32_t* d_err, cudaStream_t s)
+{
+    SO_PROFILE("csr_flat_sgd", s);
+    launch(k_csr_flat<FlatSgdOp>, dim3(flat_grid(nnz)), dim3(kBlock), s, cols, vals, ent_row, nullptr, c, nnz,
+           FlatSgdOp{P}, d_err);
     return cudaGetLastError();
 }
 

@@ -242,8 +242,9 @@ def test_csr_adam_fullsize(cuda_lib, cfg):
     m[sel], v[sel] = dev(m0), dev(v0)
     ls = G.zeros(w.rows * w.cols if per_coord else w.rows, torch.int64)
     err = G.error_word()
-    # the full-row workload gets the workspace the benchmark passes (its rows then take the row kernel)
-    ws = None if per_coord else G.workspace(so, w.lookups + 1, 1, w.rows)
+    # the workspace the benchmark passes: full rows then take the row kernel, element entries the flat update
+    ws = G.workspace(so, w.lookups * w.csr_cols_per_row + 64, 1, w.rows) if per_coord else \
+        G.workspace(so, w.lookups + 1, 1, w.rows)
     cfgc = so.AdamConfig(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps)
     ohp = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps)
     layout = so.LAST_STEP_PER_COORD if per_coord else so.LAST_STEP_PER_ROW

@@ -158,7 +158,7 @@ def _run_adam(so, R, c, steps, mode, gen, form, layout=None, hp=ADAM, check_ever
     touched = np.zeros((R, c), bool)
     ws = None
     if form == "csr" and csr_ws:
-        ws = G.workspace(so, max(g[1].shape[0] for g in grads) // c + 1, 1, R)
+        ws = G.workspace(so, max(g[1].shape[0] for g in grads) + 64, 1, R)
     for s in range(steps):
         t = s + 1
         g = grads[s]
@@ -250,12 +250,15 @@ def _csr_elem(rng, R, c, nrows, k):
     return row_off, cols, rng.standard_normal(cols.shape[0]).astype(np.float32)
 
 
+@pytest.mark.parametrize("csr_ws", [False, True], ids=["csr_kernel", "flat"])
 @pytest.mark.parametrize("mode", [0, 1], ids=["lazy", "dormancy_decay"])
 @pytest.mark.parametrize("R,c,nrows,k", [(2000, 256, 300, 16), (5000, 7, 1200, 3), (64, 40, 64, 40)])
-def test_adam_csr_element_granular(cuda_lib, mode, R, c, nrows, k):
+def test_adam_csr_element_granular(cuda_lib, mode, R, c, nrows, k, csr_ws):
+    """Element-granular CSR with a per-coordinate last_step, through the CSR kernel (no workspace) and
+    through the flat one-entry-per-thread update (workspace given; the check records rows and gaps)."""
     so = cuda_lib
     _run_adam(so, R, c, 5, mode, lambda s: _csr_elem(np.random.default_rng(4000 + s), R, c, nrows, k), "csr",
-              layout=so.LAST_STEP_PER_COORD, check_every=True)
+              layout=so.LAST_STEP_PER_COORD, check_every=True, csr_ws=csr_ws)
 
 
 @pytest.mark.parametrize("csr_ws", [False, True], ids=["csr_kernel", "row_path"])
@@ -300,7 +303,7 @@ def test_adam_weight_decay(cuda_lib, wd_mode, mode, form):
 
     f = "csr" if form.startswith("csr") else form
     layout = so.LAST_STEP_PER_COORD if form == "csr_elem" else so.LAST_STEP_PER_ROW
-    _run_adam(so, R, c, 4, mode, gen, f, layout=layout, hp=hp, check_every=True, csr_ws=(form == "csr_full"))
+    _run_adam(so, R, c, 4, mode, gen, f, layout=layout, hp=hp, check_every=True, csr_ws=form.startswith("csr"))
 
 
 def test_adam_weight_decay_bad_settings_rejected(cuda_lib):
@@ -465,21 +468,26 @@ def test_sgd_1d_canonical_and_csr(cuda_lib):
     assert int(err.item()) == 0
     assert_state_close("p", host(p), op)
     assert_state_close("buf", host(buf), ob)
-    # SparseSgdTable with an element-granular CSR gradient
+    # SparseSgdTable with an element-granular CSR gradient: the CSR kernel (no workspace) and the
+    # flat one-entry-per-thread update (workspace given)
     R, c = 3000, 20
-    rng = np.random.default_rng(2)
-    t0 = rng.standard_normal((R, c)).astype(np.float32)
-    tp, tb = dev(t0), torch.zeros((R, c), device="cuda")
-    tq, tbq = t0.copy(), np.zeros_like(t0)
-    for s in range(3):
-        ro, co, va = _csr_elem(rng, R, c, 400, 5)
-        so.check(so.sparse_sgd_table_step(tp, tb, R, c, so.csr(dev(ro), dev(co), dev(va)), cfg, None, err))
-        assert oracle.sgd_table_step(tq, tbq, row_off=ro, cols=co, vals=va, lr=w.lr, momentum=w.momentum,
-                                     weight_decay=w.weight_decay) == 0
-        torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    assert_state_close("p", host(tp), tq)
-    assert_state_close("buf", host(tb), tbq)
+    for with_ws in (False, True):
+        rng = np.random.default_rng(2)
+        t0 = rng.standard_normal((R, c)).astype(np.float32)
+        G = Guarded(seed=17)
+        tp, tb = G.array(t0), G.zeros((R, c))
+        tq, tbq = t0.copy(), np.zeros_like(t0)
+        ws = G.workspace(so, 400 * 5 + 64, 1, R) if with_ws else None
+        for s in range(3):
+            ro, co, va = _csr_elem(rng, R, c, 400, 5)
+            so.check(so.sparse_sgd_table_step(tp, tb, R, c, so.csr(G.array(ro), G.array(co), G.array(va)), cfg, ws,
+                                              err))
+            assert oracle.sgd_table_step(tq, tbq, row_off=ro, cols=co, vals=va, lr=w.lr, momentum=w.momentum,
+                                         weight_decay=w.weight_decay) == 0
+            G.check(f"sgd csr step {s + 1}")
+        assert int(err.item()) == 0
+        assert_state_close("p", host(tp), tq)
+        assert_state_close("buf", host(tb), tbq)
 
 
 # ------------------------------------------------------------------ conversions
