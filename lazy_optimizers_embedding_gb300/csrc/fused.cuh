@@ -67,6 +67,10 @@ constexpr int kTicket = SO_TICKET;
 constexpr int kRowIlp = SO_ROW_ILP;
 constexpr int kLongIlp = SO_LONG_ILP;   // gradient rows requested at once in a long piece (unstaged shapes)
 constexpr int kCombineBlock = 128;
+// Combine groups staged through shared memory (1) or merged from registers only (0).
+#ifndef SO_COMBINE_STAGED
+#define SO_COMBINE_STAGED 1
+#endif
 constexpr int kCombineIlp = SO_COMBINE_ILP;
 
 struct PieceInfo {
@@ -867,9 +871,11 @@ struct SlotRun {
 // one round trip.
 constexpr int kCombineCols = kCombineBlock;
 constexpr int kCombinePairs = kGroup;
-__host__ __device__ constexpr size_t combine_stage_bytes()
+// Row stride of the stage: the columns of a round, min(c, kCombineCols) (c % 4 == 0).
+__host__ __device__ constexpr int64_t combine_stage_width(int64_t c) { return c < kCombineCols ? c : kCombineCols; }
+__host__ __device__ constexpr size_t combine_stage_bytes(int64_t c)
 {
-    return static_cast<size_t>(kCombinePairs) * 2 * kCombineCols * sizeof(float);
+    return static_cast<size_t>(kCombinePairs) * 2 * static_cast<size_t>(combine_stage_width(c)) * sizeof(float);
 }
 
 // Merges the pairs of `run`, in order, at columns col0 + threadIdx.x (one column
@@ -883,6 +889,7 @@ __device__ __forceinline__ void merge_staged(const float* __restrict__ part, int
 {
     const int64_t width = (c - col0) < kCombineCols ? (c - col0) : kCombineCols;   // a multiple of 4
     const int quads = static_cast<int>(width / 4);
+    const int sw = static_cast<int>(combine_stage_width(c));   // row stride of the stage
     const uint32_t st0 = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
     for (int64_t m0 = 0; m0 < run.cnt; m0 += kCombinePairs) {
         const int k = (run.cnt - m0) < kCombinePairs ? static_cast<int>(run.cnt - m0) : kCombinePairs;
@@ -893,15 +900,15 @@ __device__ __forceinline__ void merge_staged(const float* __restrict__ part, int
             const int sc = rem / quads;
             const int q = rem - sc * quads;
             const float* src = part + run.slot(m0 + pr) * 2 * c + sc * c + col0 + 4 * q;
-            const uint32_t dst = st0 + static_cast<uint32_t>(((pr * 2 + sc) * kCombineCols + 4 * q) * 4);
+            const uint32_t dst = st0 + static_cast<uint32_t>(((pr * 2 + sc) * sw + 4 * q) * 4);
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
         }
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         __syncthreads();
         if (threadIdx.x < width) {
             for (int r = 0; r < k; ++r) {
-                const float xs = stage[(r * 2) * kCombineCols + threadIdx.x];
-                const float xc = stage[(r * 2 + 1) * kCombineCols + threadIdx.x];
+                const float xs = stage[(r * 2) * sw + threadIdx.x];
+                const float xc = stage[(r * 2 + 1) * sw + threadIdx.x];
                 if (m0 + r == 0) {
                     S = xs;
                     C = xc;
@@ -1071,11 +1078,14 @@ cudaError_t launch_shape(const Src& src, int64_t max_pieces, int64_t max_split, 
     if (max_split > 0) {
         SO_PROFILE(Epi::kCombineName, s);
         const int64_t groups = nb + nb / kGroup + 2;   // bound on the combine groups
-        if (c % 4 == 0 && (reinterpret_cast<uintptr_t>(part) & 15u) == 0) {
-            static const int occ = max_blocks(k_combine_split<Src, Epi, true>, kCombineBlock, combine_stage_bytes());
+        if (SO_COMBINE_STAGED && c % 4 == 0 && (reinterpret_cast<uintptr_t>(part) & 15u) == 0) {
+            const size_t csmem = combine_stage_bytes(c);
+            static int occ_by_quads[kCombineCols / 4 + 1] = {};   // occupancy by stage width, looked up once
+            int& occ = occ_by_quads[combine_stage_width(c) / 4];
+            if (occ == 0) occ = max_blocks(k_combine_split<Src, Epi, true>, kCombineBlock, csmem);
             const int64_t gb = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(occ) * num_sms(), groups));
-            launch_smem(k_combine_split<Src, Epi, true>, dim3(static_cast<unsigned>(gb)), dim3(kCombineBlock),
-                        combine_stage_bytes(), s, src, c, epi, part, nb, d_err);
+            launch_smem(k_combine_split<Src, Epi, true>, dim3(static_cast<unsigned>(gb)), dim3(kCombineBlock), csmem,
+                        s, src, c, epi, part, nb, d_err);
         } else {
             static const int occ = max_blocks(k_combine_split<Src, Epi, false>, kCombineBlock);
             const int64_t gb = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(occ) * num_sms(), groups));
