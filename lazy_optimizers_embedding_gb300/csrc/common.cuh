@@ -74,8 +74,8 @@ constexpr int kBlock = 256;            // threads per block of every kernel here
 #define SO_PIECE_LEN 32
 #endif
 constexpr int kPieceLen = SO_PIECE_LEN;   // L: sorted entries summed by one team before a partial
-// Keys per thread of a radix pass and sorted entries per thread of run detection
-// (a multiple of 4 dividing kPieceLen): kSortItems / kRunItems below kLargeN
+// Keys per thread of a radix pass and sorted warp rows per thread of run
+// detection (at most 21): kSortItems / kRunItems below kLargeN
 // entries, the large-input sizes from kLargeN on (fewer, larger tiles shorten the
 // look-back chains of large inputs; smaller tiles start more blocks on small ones).
 #ifndef SO_SORT_ITEMS
@@ -106,6 +106,13 @@ constexpr int kHistItems = 8;          // keys a histogram thread requests at on
 #endif
 #ifndef SO_HIST_KEYS
 #define SO_HIST_KEYS 8192
+#endif
+// How a radix pass finds the lanes of a warp holding the same digit: 0 = the match
+// instruction (its cost grows with the distinct digits in the warp), 1 = eight
+// ballots (a fixed cost), 2 = each lane ORs its bit into a per-warp shared word of
+// its digit (default: fastest on uniform and on concentrated digits alike).
+#ifndef SO_RANK
+#define SO_RANK 2
 #endif
 #ifndef SO_RADIX_LOOK
 #define SO_RADIX_LOOK 16

@@ -179,15 +179,17 @@ __device__ __forceinline__ uint32_t sum_hist(const uint32_t* __restrict__ bh, in
 // One stable counting pass over digit (key >> shift) & 255.  Tiles are taken in
 // launch order from an atomic counter, so a tile only ever waits on tiles that
 // are already running.  Per tile:
-//   1. warp-level ranking with __match_any_sync (warp w owns a contiguous run of
-//      the tile, items in order, so ranks are stable);
+//   1. warp-level ranking: the lanes holding a digit are found by each lane
+//      OR-ing its bit into a per-warp shared word of its digit (SO_RANK selects
+//      the match instruction or ballots instead); warp w owns a contiguous run
+//      of the tile, items in order, so ranks are stable;
 //   2. per-digit tile counts are published (flag 1 = aggregate), the exclusive
 //      prefix over earlier tiles is found by look-back and republished
 //      (flag 2 = inclusive); status word = count << 2 | flag;
 //   3. the tile is reordered by digit in shared memory and written out, each
 //      digit's run landing contiguously at its global offset.
 template <bool kFirst, int SI>
-__global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict__ idx64,
+__global__ void __launch_bounds__(kBlock, 2) k_radix_pass(const int64_t* __restrict__ idx64,
                                                        const uint32_t* __restrict__ kin,
                                                        const uint32_t* __restrict__ vin,
                                                        uint32_t* __restrict__ kout,
@@ -251,14 +253,38 @@ __global__ void __launch_bounds__(kBlock) k_radix_pass(const int64_t* __restrict
         dig[i] = valid ? static_cast<int>((k >> shift) & 255u) : 256;
     }
     const uint32_t lt = (1u << lane) - 1u;
+#if SO_RANK == 2
+    __shared__ uint32_t s_match[kWarps][256];
+    for (int i = lane; i < 256; i += 32) s_match[warp][i] = 0u;
+    __syncwarp();
+#endif
 #pragma unroll
     for (int i = 0; i < SI; ++i) {
         const int d = dig[i];
+#if SO_RANK == 0
         const uint32_t peers = __match_any_sync(kFull, d);
+#elif SO_RANK == 1
+        uint32_t peers = __ballot_sync(kFull, d < 256);
+#pragma unroll
+        for (int bit = 0; bit < 8; ++bit) {
+            const bool on = (d >> bit) & 1;
+            const uint32_t bb = __ballot_sync(kFull, on);
+            peers &= on ? bb : ~bb;
+        }
+#else
+        if (d < 256) atomicOr(&s_match[warp][d], 1u << lane);
+        __syncwarp();
+        const uint32_t peers = d < 256 ? s_match[warp][d] : 0u;
+#endif
         uint32_t b = 0;
         if (d < 256) b = s_wh[warp][d];
         __syncwarp();
-        if (d < 256 && lane == __ffs(peers) - 1) s_wh[warp][d] = b + __popc(peers);
+        if (d < 256 && lane == __ffs(peers) - 1) {
+            s_wh[warp][d] = b + __popc(peers);
+#if SO_RANK == 2
+            s_match[warp][d] = 0u;
+#endif
+        }
         __syncwarp();
         rank[i] = b + __popc(peers & lt);
     }
@@ -383,82 +409,100 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     const int64_t* __restrict__ ls, int ls_per_coord, int64_t c, int64_t bound, int64_t t,
     int32_t* d_err)
 {
+    // Warp-striped: warp w of tile T owns the 32*RI sorted positions from
+    // wbase = (T*kWarps + w)*32*RI, row i of them in item i (lane l holds
+    // position wbase + 32 i + l), so every load and store of a row is one
+    // coalesced warp access; neighbours come from shuffles, and positions are
+    // counted in order by ballots.  Piece boundaries (multiples of kPieceLen)
+    // are lane 0 of a row.
+    static_assert(kPieceLen == 32, "piece boundaries are lane 0 of a warp row");
+    static_assert(kShortLen > 0 && kShortLen < 32, "a long segment's test key lies in the next row at most");
+    static_assert(3 * RI <= 64, "kinds holds 3 bits per item");
     pdl_wait();
     // canonical outputs are caller memory the next call may read as its index
     // array: with any of them requested, dependents start after this grid exits
     if (idx_out == nullptr && seg_off_out == nullptr && perm_out == nullptr && d_nnz_out == nullptr) pdl_release();
     constexpr unsigned long long kValMask = (1ull << 62) - 1ull;
-    __shared__ uint32_t s_scan[kBlock / 32 + 1];
+    constexpr int kWarps = kBlock / 32;
+    __shared__ uint32_t s_warp[kWarps];
     __shared__ unsigned long long s_excl;
     __shared__ uint32_t s_tile;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
+    const int warp = tid >> 5;
     if (tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
     __syncthreads();
     const uint32_t tile = s_tile;
-    const uint32_t p0 = tile * (kBlock * RI) + tid * RI;
+    const uint32_t wbase = (tile * kWarps + warp) * (32 * RI);
+    const uint32_t lt = (1u << lane) - 1u;
 
-    uint32_t k[RI];
-    uint32_t prev = 0;
-    if (p0 < n && p0 > 0) prev = skey[p0 - 1];
-    if (p0 + RI <= n) {
-#pragma unroll
-        for (int v4 = 0; v4 < RI / 4; ++v4) {
-            const uint4 a = *reinterpret_cast<const uint4*>(skey + p0 + 4 * v4);
-            k[4 * v4] = a.x; k[4 * v4 + 1] = a.y; k[4 * v4 + 2] = a.z; k[4 * v4 + 3] = a.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < RI; ++i) k[i] = (p0 + i < n) ? skey[p0 + i] : 0u;
-    }
-    // a multiple q of kPieceLen inside a segment starts a new piece only when the
-    // segment already holds position q - kPieceLen (RI divides kPieceLen:
-    // at most the first item of a thread is such a multiple)
-    static_assert(kPieceLen % RI == 0, "piece boundaries fall on a thread's first item");
-    const bool at_boundary = (p0 < n) && (p0 % kPieceLen == 0) && p0 >= kPieceLen;
-    const uint32_t key_back = at_boundary ? skey[p0 - kPieceLen] : 0u;
-    uint32_t headm = 0, piecem = 0;
+    uint32_t k[RI], pmv[RI];
 #pragma unroll
     for (int i = 0; i < RI; ++i) {
-        const uint32_t q = p0 + i;
+        const uint32_t q = wbase + 32 * i + lane;
+        k[i] = q < n ? skey[q] : 0u;
+        pmv[i] = q < n ? sperm[q] : 0u;
+    }
+    // the row after the warp's last (lane 0 of the one after it too), the key
+    // before the warp's first position and the key kPieceLen before it
+    const uint32_t after = wbase + 32 * RI;
+    const uint32_t halo = after + lane < n ? skey[after + lane] : 0u;
+    const uint32_t halo2 = after + 32 < n ? skey[after + 32] : 0u;
+    const uint32_t kprev = (wbase > 0 && wbase < n) ? skey[wbase - 1] : 0u;
+    const uint32_t kback = (wbase >= 32 && wbase < n) ? skey[wbase - 32] : 0u;
+
+    // position q is a segment head when it is 0 or its key differs from q-1's; a
+    // piece head when it is a segment head, or a multiple of kPieceLen whose key
+    // equals the key kPieceLen before it.  A head's segment spans several pieces
+    // when the key at the first piece boundary at least kPieceLen past it (the
+    // next row's lane 0 for lane 0, the row after for the others) is its own, and
+    // is long when the key kShortLen past it is.
+    uint32_t headm = 0, piecem = 0, multim = 0, longm = 0;
+#pragma unroll
+    for (int i = 0; i < RI; ++i) {
+        const uint32_t q = wbase + 32 * i + lane;
+        const uint32_t up = __shfl_up_sync(kFull, k[i], 1);
+        const uint32_t row_before_last = (i == 0) ? kprev : __shfl_sync(kFull, k[i - 1], 31);
+        const uint32_t back = (i == 0) ? kback : __shfl_sync(kFull, k[i - 1], 0);
+        const uint32_t next_row = (i + 1 < RI) ? k[i + 1] : halo;
+        const uint32_t next0 = __shfl_sync(kFull, next_row, 0);
+        const uint32_t next1 = (i + 2 < RI) ? __shfl_sync(kFull, k[(i + 2) % RI], 0)
+                                            : (i + 2 == RI ? __shfl_sync(kFull, halo, 0) : halo2);
+        const uint32_t short_in = __shfl_down_sync(kFull, k[i], kShortLen);
+        const uint32_t short_wrap = __shfl_sync(kFull, next_row, (lane + kShortLen) & 31);
         if (q < n) {
-            const uint32_t before = (i == 0) ? prev : k[i - 1];
+            const uint32_t before = lane ? up : row_before_last;
             const bool h = (q == 0) || (k[i] != before);
+            const bool split = lane == 0 && q >= 32 && back == k[i];
             headm |= (h ? 1u : 0u) << i;
-            const bool split = (i == 0) && at_boundary && !h && key_back == k[0];
             piecem |= ((h || split) ? 1u : 0u) << i;
+            if (h) {
+                const uint32_t nxt = q - lane + (lane ? 64u : 32u);
+                const bool multi = nxt < n && (lane ? next1 : next0) == k[i];
+                const bool lng = q + kShortLen < n && (lane + kShortLen < 32 ? short_in : short_wrap) == k[i];
+                multim |= (multi ? 1u : 0u) << i;
+                longm |= (lng ? 1u : 0u) << i;
+            }
         }
     }
-    // everything the items below read is requested before the scan and the
-    // look-back, whose round trips it then overlaps: input positions, the key at
-    // the next piece boundary of each segment head, last_step
-    uint32_t pmv[RI];
-    if (p0 + RI <= n) {
-#pragma unroll
-        for (int v4 = 0; v4 < RI / 4; ++v4) {
-            const uint4 a = *reinterpret_cast<const uint4*>(sperm + p0 + 4 * v4);
-            pmv[4 * v4] = a.x; pmv[4 * v4 + 1] = a.y; pmv[4 * v4 + 2] = a.z; pmv[4 * v4 + 3] = a.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < RI; ++i) pmv[i] = (p0 + i < n) ? sperm[p0 + i] : 0u;
-    }
-    uint32_t nxt_key[RI], long_key[RI];
+    // last_step of each head's row (the step-order check), requested before the
+    // scan and the look-back, whose round trips it overlaps
     int64_t last[RI];
 #pragma unroll
-    for (int i = 0; i < RI; ++i) {
-        const uint32_t q = p0 + i;
-        const bool h = (headm >> i) & 1u;
-        // first boundary that can split a segment starting at q: the smallest
-        // multiple of kPieceLen that is >= q + kPieceLen
-        const uint32_t nxt = (q + 2 * kPieceLen - 1) / kPieceLen * kPieceLen;
-        nxt_key[i] = (h && nxt < n) ? skey[nxt] : ~k[i];
-        long_key[i] = (h && q + kShortLen < n) ? skey[q + kShortLen] : ~k[i];
-        last[i] = (h && ls && !ls_per_coord && static_cast<int64_t>(k[i]) < bound) ? ls[k[i]] : 0;
+    for (int i = 0; i < RI; ++i)
+        last[i] = (((headm >> i) & 1u) && ls && !ls_per_coord && static_cast<int64_t>(k[i]) < bound) ? ls[k[i]] : 0;
+
+    const uint32_t hcw = __reduce_add_sync(kFull, static_cast<unsigned>(__popc(headm)));
+    const uint32_t pcw = __reduce_add_sync(kFull, static_cast<unsigned>(__popc(piecem)));
+    if (lane == 0) s_warp[warp] = (hcw << 16) | pcw;
+    __syncthreads();
+    uint32_t wex = 0, tot = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) {
+        const uint32_t x = s_warp[w2];
+        if (w2 < warp) wex += x;
+        tot += x;
     }
-    const uint32_t hc = __popc(headm), pc = __popc(piecem);
-    uint32_t tot;
-    const uint32_t xe = block_excl_scan((hc << 16) | pc, s_scan, &tot);
     const unsigned long long agg = (static_cast<unsigned long long>(tot >> 16) << 31) | (tot & 0xffffu);
 
     if (tid < 32) {
@@ -498,57 +542,60 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     }
     __syncthreads();
     const unsigned long long ex = s_excl;
-    uint32_t h_run = static_cast<uint32_t>(ex >> 31) + (xe >> 16);       // heads before p0
-    uint32_t p_run = static_cast<uint32_t>(ex & 0x7fffffffull) + (xe & 0xffffu);
+    uint32_t h_run = static_cast<uint32_t>(ex >> 31) + (wex >> 16);      // heads before the row
+    uint32_t p_run = static_cast<uint32_t>(ex & 0x7fffffffull) + (wex & 0xffffu);
 
-    uint32_t lists[RI];   // flagged pieces of this thread, in order
-    uint64_t kinds = 0;          // 3 bits per flagged piece: long, split head, group head
-    static_assert(3 * RI <= 64, "kinds holds 3 bits per item");
+    uint32_t lists[RI];   // flagged pieces of this lane
+    uint64_t kinds = 0;   // 3 bits per flagged piece: long, split head, group head
     int nl = 0;
 #pragma unroll
     for (int i = 0; i < RI; ++i) {
-        const uint32_t q = p0 + i;
-        if (q >= n) break;
+        const uint32_t q = wbase + 32 * i + lane;
         const bool h = (headm >> i) & 1u;
-        if (h) ++h_run;
-        const uint32_t u = h_run - 1;  // segment of position q
-        if (h) {
-            seg_off[u] = q;
-            if (idx_out) idx_out[u] = static_cast<int64_t>(k[i]);
-            if (seg_off_out) seg_off_out[u] = static_cast<int64_t>(q);
-            if (ls && static_cast<int64_t>(k[i]) < bound) {
-                if (!ls_per_coord) {
-                    if (last[i] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
-                } else {
-                    const int64_t b = static_cast<int64_t>(k[i]) * c;
-                    for (int64_t jc = 0; jc < c; ++jc)
-                        if (ls[b + jc] >= t) {
-                            set_error(d_err, SPARSE_ERR_STEP_ORDER);
-                            break;
-                        }
+        const bool ph = (piecem >> i) & 1u;
+        const uint32_t hb = __ballot_sync(kFull, h);
+        const uint32_t pb = __ballot_sync(kFull, ph);
+        if (q < n) {
+            const uint32_t u = h_run + __popc(hb & lt) + (h ? 1u : 0u) - 1u;  // segment of position q
+            if (h) {
+                seg_off[u] = q;
+                if (idx_out) idx_out[u] = static_cast<int64_t>(k[i]);
+                if (seg_off_out) seg_off_out[u] = static_cast<int64_t>(q);
+                if (ls && static_cast<int64_t>(k[i]) < bound) {
+                    if (!ls_per_coord) {
+                        if (last[i] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                    } else {
+                        const int64_t b = static_cast<int64_t>(k[i]) * c;
+                        for (int64_t jc = 0; jc < c; ++jc)
+                            if (ls[b + jc] >= t) {
+                                set_error(d_err, SPARSE_ERR_STEP_ORDER);
+                                break;
+                            }
+                    }
+                }
+            }
+            const uint32_t pm = pmv[i];
+            if (perm_out) perm_out[q] = static_cast<int64_t>(pm);
+            if (ph) {
+                uint32_t flag = kMultiFlag;
+                if (h) flag = ((multim >> i) & 1u) ? kMultiFlag : (((longm >> i) & 1u) ? kLongFlag : 0u);
+                const uint32_t j = p_run + __popc(pb & lt);
+                rec[j] = make_uint4(q, k[i], u | flag, pm);
+                if (flag) {
+                    lists[nl] = j;
+                    kinds |= static_cast<uint64_t>((h && flag == kMultiFlag ? 2u : 0u) |
+                                                   (flag == kMultiFlag && (h || q % (kPieceLen * kGroup) == 0) ? 4u : 0u) |
+                                                   1u)
+                             << (3 * nl);
+                    ++nl;
                 }
             }
         }
-        const uint32_t pm = pmv[i];
-        if (perm_out) perm_out[q] = static_cast<int64_t>(pm);
-        if ((piecem >> i) & 1u) {
-            uint32_t flag = kMultiFlag;
-            if (h) flag = (nxt_key[i] == k[i]) ? kMultiFlag : (long_key[i] == k[i] ? kLongFlag : 0u);
-            rec[p_run] = make_uint4(q, k[i], u | flag, pm);
-            if (flag) {
-                lists[nl] = p_run;
-                kinds |= static_cast<uint64_t>((h && flag == kMultiFlag ? 2u : 0u) |
-                                               (flag == kMultiFlag && (h || q % (kPieceLen * kGroup) == 0) ? 4u : 0u) |
-                                               1u)
-                         << (3 * nl);
-                ++nl;
-            }
-            ++p_run;
-        }
+        h_run += __popc(hb);
+        p_run += __popc(pb);
     }
-    // the flagged pieces of the thread go to the long-piece, split-segment and
+    // the flagged pieces of the lane go to the long-piece, split-segment and
     // combine-group lists: one atomic per list and warp
-    const int lane_w = tid & 31;
 #pragma unroll
     for (int li = 0; li < 3; ++li) {
         uint32_t mine = 0;
@@ -557,11 +604,11 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(kFull, incl, o);
-            if (lane_w >= o) incl += y;
+            if (lane >= o) incl += y;
         }
         const uint32_t wtotal = __shfl_sync(kFull, incl, 31);
         uint32_t basew = 0;
-        if (lane_w == 31 && wtotal) basew = atomicAdd(counts + (li == 0 ? kCntM : li == 1 ? kCntS : kCntG), wtotal);
+        if (lane == 31 && wtotal) basew = atomicAdd(counts + (li == 0 ? kCntM : li == 1 ? kCntS : kCntG), wtotal);
         basew = __shfl_sync(kFull, basew, 31);
         uint32_t* dst = li == 0 ? mlist : li == 1 ? slist : glist;
         uint32_t at = basew + incl - mine;
