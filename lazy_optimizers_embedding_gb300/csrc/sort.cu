@@ -199,7 +199,6 @@ __global__ void __launch_bounds__(kBlock, 2) k_radix_pass(const int64_t* __restr
                                                        uint32_t* status, uint32_t* tile_ctr,
                                                        int32_t* d_err)
 {
-    pdl_enter();
     constexpr int kWarps = kBlock / 32;
     __shared__ uint32_t s_wh[kWarps][256];
     __shared__ uint32_t s_gbase[256];
@@ -212,8 +211,14 @@ __global__ void __launch_bounds__(kBlock, 2) k_radix_pass(const int64_t* __restr
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    if (tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
+    // the tile counters were zeroed by the histogram kernel, which has completed
+    // before any later pass can start (each pass waits on its predecessor before
+    // releasing its dependents): passes after the first take their tile before
+    // the wait
+    if (!kFirst && tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
     for (int i = tid; i < kWarps * 256; i += kBlock) (&s_wh[0][0])[i] = 0u;
+    pdl_enter();
+    if (kFirst && tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
     __syncthreads();
     const uint32_t tile = s_tile;
     const uint32_t base = tile * (kBlock * SI);
@@ -418,10 +423,6 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     static_assert(kPieceLen == 32, "piece boundaries are lane 0 of a warp row");
     static_assert(kShortLen > 0 && kShortLen < 32, "a long segment's test key lies in the next row at most");
     static_assert(3 * RI <= 64, "kinds holds 3 bits per item");
-    pdl_wait();
-    // canonical outputs are caller memory the next call may read as its index
-    // array: with any of them requested, dependents start after this grid exits
-    if (idx_out == nullptr && seg_off_out == nullptr && perm_out == nullptr && d_nnz_out == nullptr) pdl_release();
     constexpr unsigned long long kValMask = (1ull << 62) - 1ull;
     constexpr int kWarps = kBlock / 32;
     __shared__ uint32_t s_warp[kWarps];
@@ -430,7 +431,13 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
+    // the tile counter was zeroed by the histogram kernel, complete before the
+    // radix passes released this grid: the tile is taken before the wait
     if (tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
+    pdl_wait();
+    // canonical outputs are caller memory the next call may read as its index
+    // array: with any of them requested, dependents start after this grid exits
+    if (idx_out == nullptr && seg_off_out == nullptr && perm_out == nullptr && d_nnz_out == nullptr) pdl_release();
     __syncthreads();
     const uint32_t tile = s_tile;
     const uint32_t wbase = (tile * kWarps + warp) * (32 * RI);
@@ -595,23 +602,31 @@ __global__ void __launch_bounds__(kBlock) k_run_detect(
         p_run += __popc(pb);
     }
     // the flagged pieces of the lane go to the long-piece, split-segment and
-    // combine-group lists: one atomic per list and warp
+    // combine-group lists: one atomic per list and warp, the three in flight
+    // together (lanes 0, 1, 2)
+    uint32_t mine[3], incl[3], wtotal[3];
 #pragma unroll
     for (int li = 0; li < 3; ++li) {
-        uint32_t mine = 0;
-        for (int e = 0; e < nl; ++e) mine += static_cast<uint32_t>((kinds >> (3 * e + li)) & 1u);
-        uint32_t incl = mine;
+        mine[li] = 0;
+        for (int e = 0; e < nl; ++e) mine[li] += static_cast<uint32_t>((kinds >> (3 * e + li)) & 1u);
+        incl[li] = mine[li];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += y;
+            const uint32_t y = __shfl_up_sync(kFull, incl[li], o);
+            if (lane >= o) incl[li] += y;
         }
-        const uint32_t wtotal = __shfl_sync(kFull, incl, 31);
-        uint32_t basew = 0;
-        if (lane == 31 && wtotal) basew = atomicAdd(counts + (li == 0 ? kCntM : li == 1 ? kCntS : kCntG), wtotal);
-        basew = __shfl_sync(kFull, basew, 31);
+        wtotal[li] = __shfl_sync(kFull, incl[li], 31);
+    }
+    uint32_t basew = 0;
+    if (lane < 3) {
+        const uint32_t tot = lane == 0 ? wtotal[0] : lane == 1 ? wtotal[1] : wtotal[2];
+        if (tot) basew = atomicAdd(counts + (lane == 0 ? kCntM : lane == 1 ? kCntS : kCntG), tot);
+    }
+#pragma unroll
+    for (int li = 0; li < 3; ++li) {
+        const uint32_t b = __shfl_sync(kFull, basew, li);
         uint32_t* dst = li == 0 ? mlist : li == 1 ? slist : glist;
-        uint32_t at = basew + incl - mine;
+        uint32_t at = b + incl[li] - mine[li];
         for (int e = 0; e < nl; ++e)
             if ((kinds >> (3 * e + li)) & 1u) dst[at++] = lists[e];
     }
