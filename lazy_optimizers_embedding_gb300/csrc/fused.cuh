@@ -958,15 +958,16 @@ __device__ __forceinline__ void merge_column(const float* __restrict__ part, int
 // first), and the block of the last group to arrive merges the groups' pairs in
 // group order and applies the update.  The order of every addition is fixed by
 // the slots, whichever block arrives last, and no block waits for another.
+// Before the wait for the row kernel a block already reads its first group's
+// description (run detection's records, complete before the row kernel released
+// this grid) and its row's state (a split segment's row is written by this
+// kernel alone); only the partials need the row kernel to have finished.
 // kStaged: pairs staged through shared memory (c % 4 == 0, aligned partials).
 template <class Src, class Epi, bool kStaged>
 __global__ void __launch_bounds__(kCombineBlock, 3) k_combine_split(Src src, int64_t c, Epi epi,
                                                                     float* __restrict__ part, int64_t nb,
                                                                     int32_t* d_err)
 {
-    pdl_wait();
-    if constexpr (Epi::kEarlyRelease) pdl_release();
-    if (read_error(d_err)) return;
     constexpr int A = Epi::kArrays;
     extern __shared__ float so_combine_stage[];
     __shared__ uint32_t s_arrived;
@@ -977,29 +978,64 @@ __global__ void __launch_bounds__(kCombineBlock, 3) k_combine_split(Src src, int
             if (col0 + threadIdx.x < c) merge_column(part, c, run, col0 + threadIdx.x, S, C);
         }
     };
-    const int64_t G = src.count_groups();
-    for (int64_t t = blockIdx.x; t < G; t += gridDim.x) {
-        const PieceInfo pc = src.piece(src.group_index(t));
+    struct Group {
+        PieceInfo pc;        // the group's head piece
+        SlotRun pieces;      // the group's pieces
+        SlotRun groups;      // the segment's groups
+        int64_t ng;          // groups of the segment
+    };
+    const auto describe = [&](int64_t t) {
+        Group gr;
+        gr.pc = src.piece(src.group_index(t));
         int64_t s0, s1;
-        src.seg_bounds(pc.u(), s0, s1);
+        src.seg_bounds(gr.pc.u(), s0, s1);
         const SplitSegment seg(s0, s1);
-        const int64_t i = seg.index(pc.start);
+        const int64_t i = seg.index(gr.pc.start);
         const int64_t K = seg.pieces();
         const int64_t next = seg.group_head(seg.group(i) + 1);
         const int64_t cnt = (next < K ? next : K) - i;
         const int64_t g0 = seg.group(0);
-        const int64_t ng = seg.group(K - 1) - g0 + 1;
+        gr.ng = seg.group(K - 1) - g0 + 1;
         // this group's pieces: the first in its own slot, piece p >= 1 of the segment
         // in slot q1/kPieceLen + p - 1; the group heads after the segment's first
         // piece: group g's in slot g*kGroup
-        const SlotRun pieces{part_slot(pc.start, nb), seg.q1 / kPieceLen + i - 1, 1, cnt};
-        const SlotRun groups{part_slot(s0, nb), g0 * kGroup, kGroup, ng};
+        gr.pieces = SlotRun{part_slot(gr.pc.start, nb), seg.q1 / kPieceLen + i - 1, 1, cnt};
+        gr.groups = SlotRun{part_slot(s0, nb), g0 * kGroup, kGroup, gr.ng};
+        return gr;
+    };
+    // the row's state at columns col0 + threadIdx.x
+    const auto load_row = [&](const PieceInfo& pc, int64_t col0, float (&x)[A][1]) {
+        const int64_t col = col0 + threadIdx.x;
+        if (col < c) {
+#pragma unroll
+            for (int a = 0; a < A; ++a)
+                if (a < epi.arrays()) x[a][0] = epi.array(a)[epi.base(pc) + col];
+        }
+    };
+    const int64_t G = src.count_groups();
+    Group first{};
+    float x0[A][1];
+    int64_t last0 = 0;
+    if (static_cast<int64_t>(blockIdx.x) < G) {
+        first = describe(blockIdx.x);
+        load_row(first.pc, 0, x0);
+        const int64_t* lp = epi.stage_last(first.pc);
+        if (lp) last0 = *lp;
+    }
+    pdl_wait();
+    if constexpr (Epi::kEarlyRelease) pdl_release();
+    if (read_error(d_err)) return;
+    for (int64_t t = blockIdx.x; t < G; t += gridDim.x) {
+        const bool is_first = t == static_cast<int64_t>(blockIdx.x);
+        const Group gr = is_first ? first : describe(t);
+        const PieceInfo& pc = gr.pc;
+        const int64_t ng = gr.ng;
         if (ng > 1) {
-            if (cnt > 1) {
-                float* pd = part + pieces.first * 2 * c;
+            if (gr.pieces.cnt > 1) {
+                float* pd = part + gr.pieces.first * 2 * c;
                 for (int64_t col0 = 0; col0 < c; col0 += kCombineCols) {
                     float S, C;
-                    merge(pieces, col0, S, C);
+                    merge(gr.pieces, col0, S, C);
                     const int64_t col = col0 + threadIdx.x;
                     if (col < c) {
                         st_part<1>(pd + col, {S});
@@ -1009,24 +1045,28 @@ __global__ void __launch_bounds__(kCombineBlock, 3) k_combine_split(Src src, int
             }
             __threadfence();
             __syncthreads();
-            if (threadIdx.x == 0) s_arrived = atomicAdd(src.segment_counter(groups.first), 1u);
+            if (threadIdx.x == 0) s_arrived = atomicAdd(src.segment_counter(gr.groups.first), 1u);
             __syncthreads();
             if (static_cast<int64_t>(s_arrived) != ng - 1) continue;   // another group's block finishes it
             __threadfence();
         }
-        const int64_t* lp = epi.stage_last(pc);
-        const int64_t last = lp ? *lp : 0;
+        int64_t last = last0;
+        if (!is_first) {
+            const int64_t* lp = epi.stage_last(pc);
+            last = lp ? *lp : 0;
+        }
         const typename Epi::Row row = epi.make_row(pc, last);
         for (int64_t col0 = 0; col0 < c; col0 += kCombineCols) {
             const int64_t col = col0 + threadIdx.x;
             float x[A][1];
-            if (col < c) {
+            if (is_first && col0 == 0) {
 #pragma unroll
-                for (int a = 0; a < A; ++a)
-                    if (a < epi.arrays()) x[a][0] = epi.array(a)[epi.base(pc) + col];
+                for (int a = 0; a < A; ++a) x[a][0] = x0[a][0];
+            } else {
+                load_row(pc, col0, x);
             }
             float S, C;
-            merge(ng > 1 ? groups : pieces, col0, S, C);
+            merge(ng > 1 ? gr.groups : gr.pieces, col0, S, C);
             if (col < c) {
                 const float g[1] = {__fadd_rn(S, C)};
                 epi.template apply<1>(row, col, x, g);
