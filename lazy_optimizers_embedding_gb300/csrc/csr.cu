@@ -102,22 +102,17 @@ __device__ __forceinline__ unsigned full_row_mask(const Group& G, int64_t r0, in
 // Lane l of the warp's k-th full row (k < popc(mask)).
 __device__ __forceinline__ int nth_row(unsigned mask, int k) { return static_cast<int>(__fns(mask, 0, k + 1)); }
 
-// Validation of a CSR gradient (and of last_step < t on its touched coordinates).
-// With rows_list (only when every listed row must be full): the j-th listed row,
-// whose entries start at offset j*c, is recorded as rows_list[j], so that the
-// list with the CSR's value array is the same gradient as a canonical row-COO.
-// Offsets are validated before any slot is written, so a malformed CSR (which
-// sets *d_err) never writes outside rows_list[0 .. nnz/c).
-// With ent_row (rows not required full): every entry's row, and with ent_gap its
-// t - last_step (per-coordinate last_step; at most INT32_MAX), for the flat update.
+// Validation of a CSR gradient whose rows need not be full (and of last_step < t
+// on its touched coordinates).  With ent_row: every entry's row, and with ent_gap
+// its t - last_step (per-coordinate last_step; at most INT32_MAX), for the flat
+// update.
 template <int TQ>
 __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict__ row_off,
                                                       const int32_t* __restrict__ cols, int64_t r,
-                                                      int64_t c, int64_t nnz, int full_rows,
+                                                      int64_t c, int64_t nnz,
                                                       const int64_t* __restrict__ ls, int ls_per_coord,
-                                                      int64_t t, int64_t* __restrict__ rows_list,
-                                                      int32_t* __restrict__ ent_row, int32_t* __restrict__ ent_gap,
-                                                      int32_t* d_err)
+                                                      int64_t t, int32_t* __restrict__ ent_row,
+                                                      int32_t* __restrict__ ent_gap, int32_t* d_err)
 {
     const auto gap_of = [t](int64_t last) {
         const int64_t gap = t - last;
@@ -141,12 +136,7 @@ __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict_
             continue;
         }
         const int64_t rr = r0 + lane;
-        if (rr < r && G.b > G.a) {
-            if (full_rows && G.b - G.a != c) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
-            else if (rows_list && G.a % c == 0) rows_list[G.a / c] = rr;
-            if (ls && !ls_per_coord && ls[rr] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
-        }
-        if (full_rows) continue;   // columns checked below, entry by entry
+        if (rr < r && G.b > G.a && ls && !ls_per_coord && ls[rr] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
         const unsigned fullmask = full_row_mask<TQ>(G, r0, r, c);
         if constexpr (TQ > 0) {
             // a listed full row is canonical iff its columns are exactly 0 .. c-1
@@ -226,15 +216,65 @@ __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict_
             }
         }
     }
-    if (full_rows) {
-        // Every listed row must hold all c columns, so (the offsets being multiples of
-        // c) entry j must be column j % c: one flat pass over the column array.
-        const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
-        for (int64_t j = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; j < nnz; j += stride) {
-            const int32_t col = cols[j];
-            if (col != j % c) set_error(d_err, (col < 0 || col >= c) ? SPARSE_ERR_INDEX_OUT_OF_RANGE
-                                                                    : SPARSE_ERR_NOT_CANONICAL);
+}
+
+// Validation when every listed row must be full (per-row last_step): thread i
+// takes rows i, i + stride, ... kFullRowIlp at a time, all their offsets
+// requested together (one coalesced pair of loads per warp and row batch); a
+// non-empty row must hold exactly c entries (its start then a multiple of c,
+// the offsets starting at 0), is recorded as rows_list[start / c] and has its
+// last_step checked.  Each row's own offsets are checked to lie in [0, nnz) in
+// order before its slot is written, so a malformed CSR never writes outside
+// rows_list[0 .. nnz/c).  Then one flat pass over the column array: entry j must
+// be column j % c (four entries a thread at a time where the array is aligned).
+constexpr int kFullRowIlp = 4;
+__global__ void __launch_bounds__(kBlock) k_csr_check_full(const int64_t* __restrict__ row_off,
+                                                           const int32_t* __restrict__ cols, int64_t r, int64_t c,
+                                                           int64_t nnz, const int64_t* __restrict__ ls, int64_t t,
+                                                           int64_t* __restrict__ rows_list, int32_t* d_err)
+{
+    pdl_enter();
+    if (blockIdx.x == 0 && threadIdx.x == 0 && (row_off[0] != 0 || row_off[r] != nnz))
+        set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    for (int64_t base = i0; base < r; base += stride * kFullRowIlp) {
+        int64_t a[kFullRowIlp], b[kFullRowIlp];
+#pragma unroll
+        for (int u = 0; u < kFullRowIlp; ++u) {
+            const int64_t rr = base + u * stride;
+            a[u] = rr < r ? row_off[rr] : 0;
+            b[u] = rr < r ? row_off[rr + 1] : 0;
         }
+#pragma unroll
+        for (int u = 0; u < kFullRowIlp; ++u) {
+            const int64_t rr = base + u * stride;
+            if (rr >= r || a[u] == b[u]) continue;
+            if (a[u] < 0 || a[u] > b[u] || b[u] > nnz || b[u] - a[u] != c || a[u] % c != 0) {
+                set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
+                continue;
+            }
+            if (rows_list) rows_list[a[u] / c] = rr;
+            if (ls && ls[rr] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+        }
+    }
+    const bool vec = (reinterpret_cast<uintptr_t>(cols) & 15u) == 0;
+    const int64_t n4 = vec ? nnz / 4 : 0;
+    for (int64_t q = i0; q < n4; q += stride) {
+        const int4 v = *reinterpret_cast<const int4*>(cols + 4 * q);
+        const int32_t w[4] = {v.x, v.y, v.z, v.w};
+        int64_t want = (4 * q) % c;   // column of entry 4q, then stepped with wrap-around
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (w[e] != want)
+                set_error(d_err, (w[e] < 0 || w[e] >= c) ? SPARSE_ERR_INDEX_OUT_OF_RANGE : SPARSE_ERR_NOT_CANONICAL);
+            if (++want == c) want = 0;
+        }
+    }
+    for (int64_t j = 4 * n4 + i0; j < nnz; j += stride) {
+        const int32_t col = cols[j];
+        if (col != j % c) set_error(d_err, (col < 0 || col >= c) ? SPARSE_ERR_INDEX_OUT_OF_RANGE
+                                                                : SPARSE_ERR_NOT_CANONICAL);
     }
 }
 
@@ -405,13 +445,13 @@ struct CsrSgdOp {
 // Blocks of the CSR kernels: one warp per group of 32 rows, at most
 // SO_CSR_BLOCKS_PER_SM blocks per SM (several waves: a block that finds only
 // empty groups retires quickly and its slot takes the next block).
-// The check kernel's cap; with full rows (offsets, last_step and a flat column
-// pass only) fewer blocks, each walking more groups, measured faster.
+// The check kernel's cap.
 #ifndef SO_CSR_CHECK_BLOCKS_PER_SM
 #define SO_CSR_CHECK_BLOCKS_PER_SM SO_CSR_BLOCKS_PER_SM
 #endif
-#ifndef SO_CSR_CHECK_FULL_BLOCKS_PER_SM
-#define SO_CSR_CHECK_FULL_BLOCKS_PER_SM 4
+// Blocks per SM of the full-row check (one row per thread and pass).
+#ifndef SO_CSR_FULL_BLOCKS_PER_SM
+#define SO_CSR_FULL_BLOCKS_PER_SM 8
 #endif
 static int group_blocks(int64_t r, int per_sm = SO_CSR_BLOCKS_PER_SM)
 {
@@ -447,14 +487,18 @@ cudaError_t csr_check(const int64_t* row_off, const int32_t* cols, int64_t r, in
                       int32_t* ent_row, int32_t* ent_gap, int32_t* d_err, cudaStream_t s)
 {
     SO_PROFILE("csr_check", s);
+    if (full_rows) {
+        const int blocks = static_cast<int>(std::max<int64_t>(
+            1, std::min<int64_t>((std::max(r, nnz / 4) + kBlock - 1) / kBlock, int64_t(SO_CSR_FULL_BLOCKS_PER_SM) * num_sms())));
+        launch(k_csr_check_full, dim3(blocks), dim3(kBlock), s, row_off, cols, r, c, nnz, ls_per_coord ? nullptr : ls, t,
+               rows_list, d_err);
+        return cudaGetLastError();
+    }
     const int tq = full_row_team(c, aligned16(cols));
 #define SO_CHECK(T)                                                                                              \
     launch(k_csr_check<T>,                                                                                      \
-           dim3(group_blocks(r, full_rows ? SO_CSR_CHECK_FULL_BLOCKS_PER_SM : SO_CSR_CHECK_BLOCKS_PER_SM)),     \
-           dim3(kBlock), s, row_off, cols, r, c,                                                                 \
-           nnz, full_rows, ls,                                                                                      \
-           ls_per_coord, t, full_rows ? rows_list : nullptr, full_rows ? nullptr : ent_row,                     \
-           full_rows ? nullptr : ent_gap, d_err)
+           dim3(group_blocks(r, SO_CSR_CHECK_BLOCKS_PER_SM)),                                                   \
+           dim3(kBlock), s, row_off, cols, r, c, nnz, ls, ls_per_coord, t, ent_row, ent_gap, d_err)
     SO_TQ_DISPATCH(tq, SO_CHECK)
 #undef SO_CHECK
     return cudaGetLastError();
