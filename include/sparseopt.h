@@ -30,8 +30,11 @@
  *             programmatic dependent launch: each may be scheduled while the
  *             kernel before it on the stream finishes, and waits for it before
  *             touching memory that kernel may use.  One read comes earlier: on a
- *             raw (non-canonical) gradient, the first kernel reads the index
- *             array before that wait.  That is safe when the index array was
+ *             raw (non-canonical) gradient the first kernel reads the index
+ *             array before that wait, and on a CSR gradient under a per-row
+ *             last_step it reads the offset and column arrays (the problems it
+ *             finds reach *d_err only after the wait).  That is safe when these
+ *             arrays were
  *             written by a copy, a memset, an ordinary kernel launch, or any call
  *             of this library: every call that writes an output other than
  *             optimizer state and the error word (canonical indices, offsets,
@@ -40,8 +43,8 @@
  *             writes.  It is not safe when the index array was written by a
  *             kernel of the caller's own that releases its dependents early
  *             (programmatic dependent launch), nor when an optimizer state array
- *             (p, m, v, buf, last_step) of one call is the index array of the
- *             next call on the same stream.
+ *             (p, m, v, buf, last_step) of one call is one of those arrays of
+ *             the next call on the same stream.
  *   Errors.   Host-checkable problems (null pointer, negative size, bad config,
  *             t < 1, workspace too small, a size beyond a stated limit) return a
  *             non-zero sparse_status_t before anything is enqueued.  A failed

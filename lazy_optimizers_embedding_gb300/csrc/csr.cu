@@ -227,37 +227,38 @@ __global__ void __launch_bounds__(kBlock) k_csr_check(const int64_t* __restrict_
 // order before its slot is written, so a malformed CSR never writes outside
 // rows_list[0 .. nnz/c).  Then one flat pass over the column array: entry j must
 // be column j % c (four entries a thread at a time where the array is aligned).
+// The CSR is the call's input, so the first batch of offsets and the column pass
+// are read and checked before the wait for the previous kernel on the stream; the
+// problems found are only recorded then and written to *d_err after the wait (a
+// previous kernel may still read the error word), as are rows_list (workspace
+// the previous kernel may use) and the last_step checks (last_step it may write).
 constexpr int kFullRowIlp = 4;
 __global__ void __launch_bounds__(kBlock) k_csr_check_full(const int64_t* __restrict__ row_off,
                                                            const int32_t* __restrict__ cols, int64_t r, int64_t c,
                                                            int64_t nnz, const int64_t* __restrict__ ls, int64_t t,
                                                            int64_t* __restrict__ rows_list, int32_t* d_err)
 {
-    pdl_enter();
-    if (blockIdx.x == 0 && threadIdx.x == 0 && (row_off[0] != 0 || row_off[r] != nnz))
-        set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
     const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
-    for (int64_t base = i0; base < r; base += stride * kFullRowIlp) {
-        int64_t a[kFullRowIlp], b[kFullRowIlp];
+    int bad = 0;   // SPARSE_ERR_NOT_CANONICAL or SPARSE_ERR_INDEX_OUT_OF_RANGE found before the wait
+    if (i0 == 0 && (row_off[0] != 0 || row_off[r] != nnz)) bad = SPARSE_ERR_NOT_CANONICAL;
+    const auto load = [&](int64_t base, int64_t (&a)[kFullRowIlp], int64_t (&b)[kFullRowIlp]) {
 #pragma unroll
         for (int u = 0; u < kFullRowIlp; ++u) {
             const int64_t rr = base + u * stride;
             a[u] = rr < r ? row_off[rr] : 0;
             b[u] = rr < r ? row_off[rr + 1] : 0;
         }
+    };
+    // a row is taken (listed and checked) when its offsets are well formed
+    const auto well_formed = [&](int64_t a, int64_t b) {
+        return a >= 0 && a <= b && b <= nnz && b - a == c && a % c == 0;
+    };
+    int64_t a0[kFullRowIlp], b0[kFullRowIlp];
+    load(i0, a0, b0);
 #pragma unroll
-        for (int u = 0; u < kFullRowIlp; ++u) {
-            const int64_t rr = base + u * stride;
-            if (rr >= r || a[u] == b[u]) continue;
-            if (a[u] < 0 || a[u] > b[u] || b[u] > nnz || b[u] - a[u] != c || a[u] % c != 0) {
-                set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
-                continue;
-            }
-            if (rows_list) rows_list[a[u] / c] = rr;
-            if (ls && ls[rr] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
-        }
-    }
+    for (int u = 0; u < kFullRowIlp; ++u)
+        if (i0 + u * stride < r && a0[u] != b0[u] && !well_formed(a0[u], b0[u])) bad = SPARSE_ERR_NOT_CANONICAL;
     const bool vec = (reinterpret_cast<uintptr_t>(cols) & 15u) == 0;
     const int64_t n4 = vec ? nnz / 4 : 0;
     for (int64_t q = i0; q < n4; q += stride) {
@@ -266,15 +267,33 @@ __global__ void __launch_bounds__(kBlock) k_csr_check_full(const int64_t* __rest
         int64_t want = (4 * q) % c;   // column of entry 4q, then stepped with wrap-around
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            if (w[e] != want)
-                set_error(d_err, (w[e] < 0 || w[e] >= c) ? SPARSE_ERR_INDEX_OUT_OF_RANGE : SPARSE_ERR_NOT_CANONICAL);
+            if (w[e] != want) bad = (w[e] < 0 || w[e] >= c) ? SPARSE_ERR_INDEX_OUT_OF_RANGE : SPARSE_ERR_NOT_CANONICAL;
             if (++want == c) want = 0;
         }
     }
     for (int64_t j = 4 * n4 + i0; j < nnz; j += stride) {
         const int32_t col = cols[j];
-        if (col != j % c) set_error(d_err, (col < 0 || col >= c) ? SPARSE_ERR_INDEX_OUT_OF_RANGE
-                                                                : SPARSE_ERR_NOT_CANONICAL);
+        if (col != j % c) bad = (col < 0 || col >= c) ? SPARSE_ERR_INDEX_OUT_OF_RANGE : SPARSE_ERR_NOT_CANONICAL;
+    }
+    pdl_enter();
+    if (bad) set_error(d_err, bad);
+    const auto take = [&](int64_t base, const int64_t (&a)[kFullRowIlp], const int64_t (&b)[kFullRowIlp]) {
+#pragma unroll
+        for (int u = 0; u < kFullRowIlp; ++u) {
+            const int64_t rr = base + u * stride;
+            if (rr >= r || a[u] == b[u] || !well_formed(a[u], b[u])) continue;
+            if (rows_list) rows_list[a[u] / c] = rr;
+            if (ls && ls[rr] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+        }
+    };
+    take(i0, a0, b0);
+    for (int64_t base = i0 + stride * kFullRowIlp; base < r; base += stride * kFullRowIlp) {
+        int64_t a[kFullRowIlp], b[kFullRowIlp];
+        load(base, a, b);
+#pragma unroll
+        for (int u = 0; u < kFullRowIlp; ++u)
+            if (base + u * stride < r && a[u] != b[u] && !well_formed(a[u], b[u])) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
+        take(base, a, b);
     }
 }
 

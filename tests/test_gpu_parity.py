@@ -613,7 +613,7 @@ def test_errors_set_d_err_and_write_nothing(cuda_lib):
     at40 = [0 if i <= 40 else c for i in range(R + 1)]      # row 40: last_step 9 >= t
     assert step(csr_case(at40, list(range(c)))) == so.ERR_STEP_ORDER
     shifted = [1 if i <= 3 else c + 1 for i in range(R + 1)]  # offsets not starting at 0
-    assert step(csr_case(shifted, list(range(c + 1)))) == so.ERR_NOT_CANONICAL
+    assert step(csr_case(shifted, [0] + list(range(c)))) == so.ERR_NOT_CANONICAL   # columns all in range
     lsc = dev(np.zeros(R * c, np.int64))
     unordered = [0, 0, 0, 0] + [2] * (R - 3)
     assert step(csr_case(unordered, [5, 1]), layout=so.LAST_STEP_PER_COORD, lsv=lsc) == so.ERR_NOT_CANONICAL
