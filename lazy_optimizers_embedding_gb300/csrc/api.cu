@@ -307,6 +307,8 @@ sparse_status_t sparse_sgd_table_step(float* p, float* buf, int64_t r, int64_t c
     if (n == 0) return SPARSE_OK;
     const int vec4 = (c % 4 == 0) && aligned16(p) && (buf == nullptr || aligned16(buf)) && aligned16(grad->vals);
     if (grad->is_canonical) {
+        if (c == 1 && n <= kSmallCanonMax)   // check and update in one launch
+            return from_cuda(small_canon_sgd(grad->row_idx, n, r, grad->vals, P, d_err, stream));
         e = check_canonical_rows(grad->row_idx, n, r, c, nullptr, 0, 0, d_err, stream);
         if (e == cudaSuccess) e = fused_rows_sgd_canon(grad->row_idx, n, grad->vals, c, P, vec4, d_err, stream);
         return from_cuda(e);

@@ -319,6 +319,12 @@ cudaError_t fused_rows_sgd_canon(const int64_t* rows, int64_t n, const float* va
                                  const SgdParams& P, int vec4, int32_t* d_err, cudaStream_t s);
 cudaError_t fused_rows_store_sorted(const SortWs& ws, const WsLayout& L, const float* vals, int64_t c,
                                     const StoreParams& P, int vec4, int32_t* d_err, cudaStream_t s);
+// A canonical 1-D SGD step (c == 1) of at most 4,096 entries: check and update in
+// one single-block launch (for Adam the check and the row kernel as two launches
+// measured as fast or faster, so Adam keeps them).
+constexpr int64_t kSmallCanonMax = 4096;
+cudaError_t small_canon_sgd(const int64_t* rows, int64_t n, int64_t r, const float* vals, const SgdParams& P,
+                            int32_t* d_err, cudaStream_t s);
 
 // CSR (element-granular) paths.
 // rows_list (full_rows only, may be NULL): filled with the listed rows; ent_row /

@@ -1077,6 +1077,74 @@ __global__ void __launch_bounds__(kCombineBlock, 3) k_combine_split(Src src, int
     }
 }
 
+// A small canonical 1-D step (one coordinate per entry, at most kSmallCanon
+// entries) in one block and one launch: every entry is checked (index in range,
+// strictly ascending, last_step < t) while its state, last_step and gradient are
+// read, the block waits at a barrier, and only if the error word is still clear
+// is any coordinate written, so the step stays all-or-nothing without a second
+// launch.
+constexpr int kSmallCanonBlock = 1024;
+constexpr int kSmallCanonPer = 4;   // entries a thread
+constexpr int64_t kSmallCanon = static_cast<int64_t>(kSmallCanonPer) * kSmallCanonBlock;
+static_assert(kSmallCanon == kSmallCanonMax, "the host switch and the kernel agree on the size");
+template <class Epi>
+__global__ void __launch_bounds__(kSmallCanonBlock) k_small_canon(const int64_t* __restrict__ rows, int64_t n,
+                                                                   int64_t r, const float* __restrict__ vals,
+                                                                   Epi epi, const int64_t* __restrict__ ls,
+                                                                   int64_t t, int32_t* d_err)
+{
+    constexpr int A = Epi::kArrays;
+    pdl_enter();
+    PieceInfo pc[kSmallCanonPer];
+    float x[kSmallCanonPer][A][1], g[kSmallCanonPer][1];
+    int64_t last[kSmallCanonPer];
+    bool live[kSmallCanonPer];
+#pragma unroll
+    for (int j = 0; j < kSmallCanonPer; ++j) {
+        const int64_t i = threadIdx.x + static_cast<int64_t>(j) * kSmallCanonBlock;
+        live[j] = false;
+        if (i >= n) continue;
+        const int64_t k = rows[i];
+        if (k < 0 || k >= r) {
+            set_error(d_err, SPARSE_ERR_INDEX_OUT_OF_RANGE);
+            continue;
+        }
+        if (i > 0 && rows[i - 1] >= k) set_error(d_err, SPARSE_ERR_NOT_CANONICAL);
+        live[j] = true;
+        pc[j].start = static_cast<uint32_t>(i);
+        pc[j].end = static_cast<uint32_t>(i + 1);
+        pc[j].key = static_cast<uint32_t>(k);
+        pc[j].uf = static_cast<uint32_t>(i) & kSingleMask;
+        pc[j].perm0 = static_cast<uint32_t>(i);
+#pragma unroll
+        for (int a = 0; a < A; ++a)
+            if (a < epi.arrays()) x[j][a][0] = epi.array(a)[epi.base(pc[j])];
+        g[j][0] = vals[i];
+        const int64_t* lp = epi.stage_last(pc[j]);
+        last[j] = lp ? *lp : 0;
+        if (ls && ls[k] >= t) set_error(d_err, SPARSE_ERR_STEP_ORDER);
+    }
+    __syncthreads();
+    if (read_error(d_err)) return;
+    const unsigned self = 1u << (threadIdx.x & 31);
+#pragma unroll
+    for (int j = 0; j < kSmallCanonPer; ++j) {
+        if (!live[j]) continue;
+        const typename Epi::Row row = epi.make_row(pc[j], last[j]);
+        epi.template apply<1>(row, 0, x[j], g[j]);
+        epi.end_row(row, 0, self);
+    }
+}
+
+template <class Epi>
+cudaError_t launch_small_canon(const int64_t* rows, int64_t n, int64_t r, const float* vals, const Epi& epi,
+                               const int64_t* ls, int64_t t, int32_t* d_err, cudaStream_t s)
+{
+    SO_PROFILE(Epi::kName, s);
+    launch(k_small_canon<Epi>, dim3(1), dim3(kSmallCanonBlock), s, rows, n, r, vals, epi, ls, t, d_err);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------ launch
 template <class K>
 int max_blocks(K kernel, int threads, size_t smem = 0)

@@ -17,4 +17,10 @@ cudaError_t fused_rows_sgd_canon(const int64_t* rows, int64_t n, const float* va
     return launch_fused(CanonSrc{rows, n}, n, 0, vals, c, SgdEpi{P, c}, nullptr, 0, vec4, d_err, s);
 }
 
+cudaError_t small_canon_sgd(const int64_t* rows, int64_t n, int64_t r, const float* vals, const SgdParams& P,
+                            int32_t* d_err, cudaStream_t s)
+{
+    return launch_small_canon(rows, n, r, vals, SgdEpi{P, 1}, nullptr, 0, d_err, s);
+}
+
 }  // namespace so

@@ -406,6 +406,85 @@ def test_adam_1d(cuda_lib, mode, canonical):
     assert np.array_equal(host(ls), ols)
 
 
+@pytest.mark.parametrize("n", [1, 1000, 4096, 4097])
+@pytest.mark.parametrize("opt", ["adam_lazy", "adam_dd", "sgd"])
+def test_canonical_1d_single_launch_boundary(cuda_lib, n, opt):
+    """Canonical 1-D SGD steps of up to 4,096 entries take one single-block launch (check,
+    barrier, update), 4,097 the check and row kernels; Adam steps take the two launches at every
+    size.  All match the oracle, leave untouched coordinates (special values planted) bit for bit
+    and stay inside their guard regions, and failed steps write nothing."""
+    so = cuda_lib
+    dim = 60_000
+    rng = np.random.default_rng(n + len(opt))
+    p0 = (rng.standard_normal(dim) * 0.01).astype(np.float32)
+    steps = []
+    for s in range(3):
+        idx = np.sort(rng.choice(dim, n, replace=False)).astype(np.int64)
+        steps.append((idx, (rng.standard_normal(n) * 0.01).astype(np.float32)))
+    never = np.ones(dim, bool)
+    for idx, _ in steps:
+        never[idx] = False
+    srng = np.random.default_rng(3)
+    plant_specials(p0, never, srng)
+    G = Guarded(seed=n)
+    err = G.error_word()
+    touched = ~never
+    if opt == "sgd":
+        b0 = np.zeros(dim, np.float32)
+        plant_specials(b0, never, srng)
+        p, buf = G.array(p0), G.array(b0)
+        op, ob = p0.copy(), b0.copy()
+        cfg = so.SgdConfig(lr=0.05, momentum=0.9, weight_decay=1e-4)
+        for idx, g in steps:
+            so.check(so.sparse_sgd_step(p, buf, dim, G.array(idx), G.array(g), n, 1, cfg, None, err))
+            assert oracle.sgd_step(op, ob, idx, g, lr=0.05, momentum=0.9, weight_decay=1e-4) == 0
+            G.check("sgd 1-D")
+        assert int(err.item()) == 0
+        assert_state_close("p", host(p), op, touched, p0)
+        assert_state_close("buf", host(buf), ob, touched, b0)
+        return
+    mode = so.DORMANCY_DECAY if opt == "adam_dd" else so.LAZY
+    omode = oracle.MODE_DORMANCY_DECAY if opt == "adam_dd" else oracle.MODE_LAZY
+    m0 = np.zeros(dim, np.float32)
+    v0 = np.zeros(dim, np.float32)
+    plant_specials(m0, never, srng)
+    plant_specials(v0, never, srng)
+    p, m, v = G.array(p0), G.array(m0), G.array(v0)
+    ls = G.array(np.zeros(dim, np.int64))
+    op, om, ov, ols = p0.copy(), m0.copy(), v0.copy(), np.zeros(dim, np.int64)
+    cfg = so.AdamConfig(**ADAM)
+    for s, (idx, g) in enumerate(steps):
+        t = 2 * s + 1
+        so.check(so.sparse_adam_step(p, m, v, ls, dim, G.array(idx), G.array(g), n, 1, t, cfg, mode, None, err))
+        assert oracle.adam_step(op, om, ov, ols, idx, g, t, mode=omode, **ADAM) == 0
+        G.check("adam 1-D")
+    assert int(err.item()) == 0
+    assert_state_close("p", host(p), op, touched, p0)
+    assert_state_close("m", host(m), om, touched, m0)
+    assert_state_close("v", host(v), ov, touched, v0)
+    assert np.array_equal(host(ls), ols)
+    # errors on the same path: nothing written, the code set
+    if n < 2:
+        return
+    before = [host(a).copy() for a in (p, m, v, ls)]
+    idx0 = steps[0][0]
+    g0 = steps[0][1]
+    bad_cases = [(np.concatenate([idx0[:-1], [dim]]), so.ERR_INDEX_OUT_OF_RANGE),
+                 (np.concatenate([idx0[:1], idx0[:-1]]), so.ERR_NOT_CANONICAL)]
+    for bad, want in bad_cases:
+        e = G.error_word()
+        so.check(so.sparse_adam_step(p, m, v, ls, dim, G.array(bad.astype(np.int64)), G.array(g0), n, 1, 100, cfg,
+                                     mode, None, e))
+        assert int(e.item()) == want
+    e = G.error_word()   # t not above the last_step of a listed coordinate
+    so.check(so.sparse_adam_step(p, m, v, ls, dim, G.array(steps[-1][0]), G.array(g0), n, 1, 2 * 2 + 1, cfg, mode,
+                                 None, e))
+    assert int(e.item()) == so.ERR_STEP_ORDER
+    G.check("adam 1-D errors")
+    for name, a, b in zip(("p", "m", "v", "last_step"), (p, m, v, ls), before):
+        assert host(a).tobytes() == b.tobytes(), f"{name} written by a failed step"
+
+
 # ------------------------------------------------------------------ lazy SGD
 @pytest.mark.parametrize("R,c,mom,wd", [(20000, 32, 0.9, 1e-4), (5000, 1, 0.9, 0.0), (3000, 128, 0.0, 0.0),
                                         (4000, 6, 0.5, 0.1)])
