@@ -43,6 +43,8 @@ CANON_CASES = [
     (70_000, 2, 100_000, 0),
     (600_000, 1, 2_000_000, 3000),   # large-input tiles (16 keys per thread), 21-bit keys
     (530_000, 4, 40_000_000, 0),     # large-input tiles, 26-bit keys (four passes)
+    (5000, 2, 2**32, 300),           # 32-bit keys at the bound's cap, hot key 2^32 - 1 (all bits set)
+    (3000, 1, 2**31 + 7, 0),         # keys above 2^31
 ]
 
 
@@ -93,6 +95,10 @@ def test_canonicalize_empty_and_deterministic(cuda_lib):
     so.check(so.sparse_canonicalize(e, torch.empty(0, device="cuda"), 0, 4, 10, e, None, seg, None, nnz, None, err))
     torch.cuda.synchronize()
     assert int(nnz.item()) == 0 and int(seg.item()) == 0
+    # keys are 32-bit: a bound above 2^32 is refused on the host, before anything is enqueued
+    one = torch.zeros(1, dtype=torch.int64, device="cuda")
+    assert so.sparse_canonicalize(one, torch.zeros(1, device="cuda"), 1, 1, 2**32 + 1, one, None, None, None, nnz,
+                                  so.workspace(1, 1, 2**32), err) == so.ERR_INVALID_ARG
     rng = np.random.default_rng(3)
     n, c, bound = 30000, 64, 2000
     idx = _raw_rows(rng, n, bound, hot=5, hot_count=9000)
