@@ -107,13 +107,6 @@ constexpr int kHistItems = 8;          // keys a histogram thread requests at on
 #ifndef SO_HIST_KEYS
 #define SO_HIST_KEYS 8192
 #endif
-// How a radix pass finds the lanes of a warp holding the same digit: 0 = the match
-// instruction (its cost grows with the distinct digits in the warp), 1 = eight
-// ballots (a fixed cost), 2 = each lane ORs its bit into a per-warp shared word of
-// its digit (default: fastest on uniform and on concentrated digits alike).
-#ifndef SO_RANK
-#define SO_RANK 2
-#endif
 #ifndef SO_RADIX_LOOK
 #define SO_RADIX_LOOK 16
 #endif

@@ -180,9 +180,10 @@ __device__ __forceinline__ uint32_t sum_hist(const uint32_t* __restrict__ bh, in
 // launch order from an atomic counter, so a tile only ever waits on tiles that
 // are already running.  Per tile:
 //   1. warp-level ranking: the lanes holding a digit are found by each lane
-//      OR-ing its bit into a per-warp shared word of its digit (SO_RANK selects
-//      the match instruction or ballots instead); warp w owns a contiguous run
-//      of the tile, items in order, so ranks are stable;
+//      OR-ing its bit into a per-warp shared word of its digit (a fixed cost,
+//      where a match instruction's grows with the distinct digits in the warp);
+//      warp w owns a contiguous run of the tile, items in order, so ranks are
+//      stable;
 //   2. per-digit tile counts are published (flag 1 = aggregate), the exclusive
 //      prefix over earlier tiles is found by look-back and republished
 //      (flag 2 = inclusive); status word = count << 2 | flag;
@@ -258,37 +259,21 @@ __global__ void __launch_bounds__(kBlock, 2) k_radix_pass(const int64_t* __restr
         dig[i] = valid ? static_cast<int>((k >> shift) & 255u) : 256;
     }
     const uint32_t lt = (1u << lane) - 1u;
-#if SO_RANK == 2
     __shared__ uint32_t s_match[kWarps][256];
     for (int i = lane; i < 256; i += 32) s_match[warp][i] = 0u;
     __syncwarp();
-#endif
 #pragma unroll
     for (int i = 0; i < SI; ++i) {
         const int d = dig[i];
-#if SO_RANK == 0
-        const uint32_t peers = __match_any_sync(kFull, d);
-#elif SO_RANK == 1
-        uint32_t peers = __ballot_sync(kFull, d < 256);
-#pragma unroll
-        for (int bit = 0; bit < 8; ++bit) {
-            const bool on = (d >> bit) & 1;
-            const uint32_t bb = __ballot_sync(kFull, on);
-            peers &= on ? bb : ~bb;
-        }
-#else
         if (d < 256) atomicOr(&s_match[warp][d], 1u << lane);
         __syncwarp();
         const uint32_t peers = d < 256 ? s_match[warp][d] : 0u;
-#endif
         uint32_t b = 0;
         if (d < 256) b = s_wh[warp][d];
         __syncwarp();
         if (d < 256 && lane == __ffs(peers) - 1) {
             s_wh[warp][d] = b + __popc(peers);
-#if SO_RANK == 2
             s_match[warp][d] = 0u;
-#endif
         }
         __syncwarp();
         rank[i] = b + __popc(peers & lt);
