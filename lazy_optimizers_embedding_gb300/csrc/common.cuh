@@ -99,7 +99,10 @@ constexpr int kSortItemsLarge = SO_SORT_ITEMS_LARGE;
 constexpr int kRunItemsLarge = SO_RUN_ITEMS_LARGE;
 constexpr int64_t kLargeN = SO_LARGE_N;
 constexpr int kMaxPasses = 4;          // 8-bit digits, keys < 2^32
-constexpr int kGroup = 32;             // pieces of a split segment merged by one team first
+#ifndef SO_GROUP
+#define SO_GROUP 16
+#endif
+constexpr int kGroup = SO_GROUP;       // pieces of a split segment merged by one combine block first
 constexpr int kHistItems = 8;          // keys a histogram thread requests at once
 #ifndef SO_HIST_BLOCKS
 #define SO_HIST_BLOCKS 256

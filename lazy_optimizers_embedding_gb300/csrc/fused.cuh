@@ -1190,7 +1190,12 @@ cudaError_t launch_shape(const Src& src, int64_t max_pieces, int64_t max_split, 
             const size_t csmem = combine_stage_bytes(c);
             static int occ_by_quads[kCombineCols / 4 + 1] = {};   // occupancy by stage width, looked up once
             int& occ = occ_by_quads[combine_stage_width(c) / 4];
-            if (occ == 0) occ = max_blocks(k_combine_split<Src, Epi, true>, kCombineBlock, csmem);
+            if (occ == 0) {
+                if (csmem > 48 * 1024)
+                    cudaFuncSetAttribute(k_combine_split<Src, Epi, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(csmem));
+                occ = max_blocks(k_combine_split<Src, Epi, true>, kCombineBlock, csmem);
+            }
             const int64_t gb = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(occ) * num_sms(), groups));
             launch_smem(k_combine_split<Src, Epi, true>, dim3(static_cast<unsigned>(gb)), dim3(kCombineBlock), csmem,
                         s, src, c, epi, part, nb, d_err);
