@@ -110,6 +110,10 @@ constexpr int kHistItems = 8;          // keys a histogram thread requests at on
 #ifndef SO_HIST_KEYS
 #define SO_HIST_KEYS 8192
 #endif
+// Partial pairs a combine block stages per round (0: a group's worth).
+#ifndef SO_COMBINE_PAIRS
+#define SO_COMBINE_PAIRS 0
+#endif
 #ifndef SO_RADIX_LOOK
 #define SO_RADIX_LOOK 16
 #endif

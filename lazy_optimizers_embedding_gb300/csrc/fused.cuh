@@ -867,10 +867,12 @@ struct SlotRun {
 };
 
 // Columns a combine block merges per round through its shared stage, and the
-// pairs it stages per round: one group's worth, so that merging a group costs
-// one round trip.
+// pairs it stages per round: by default one group's worth, so that merging a
+// group costs one round trip (a 16-pair stage, 16 KB at 128 columns, measured
+// faster than 32-pair ones, whose 32 KB make the SMs change their shared-memory
+// split between the row kernel and the combine).
 constexpr int kCombineCols = kCombineBlock;
-constexpr int kCombinePairs = kGroup;
+constexpr int kCombinePairs = SO_COMBINE_PAIRS > 0 ? SO_COMBINE_PAIRS : kGroup;
 // Row stride of the stage: the columns of a round, min(c, kCombineCols) (c % 4 == 0).
 __host__ __device__ constexpr int64_t combine_stage_width(int64_t c) { return c < kCombineCols ? c : kCombineCols; }
 __host__ __device__ constexpr size_t combine_stage_bytes(int64_t c)
@@ -1191,9 +1193,8 @@ cudaError_t launch_shape(const Src& src, int64_t max_pieces, int64_t max_split, 
             static int occ_by_quads[kCombineCols / 4 + 1] = {};   // occupancy by stage width, looked up once
             int& occ = occ_by_quads[combine_stage_width(c) / 4];
             if (occ == 0) {
-                if (csmem > 48 * 1024)
-                    cudaFuncSetAttribute(k_combine_split<Src, Epi, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(csmem));
+                cudaFuncSetAttribute(k_combine_split<Src, Epi, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(csmem));
                 occ = max_blocks(k_combine_split<Src, Epi, true>, kCombineBlock, csmem);
             }
             const int64_t gb = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(occ) * num_sms(), groups));
