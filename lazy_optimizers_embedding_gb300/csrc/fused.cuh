@@ -1193,8 +1193,10 @@ cudaError_t launch_shape(const Src& src, int64_t max_pieces, int64_t max_split, 
             static int occ_by_quads[kCombineCols / 4 + 1] = {};   // occupancy by stage width, looked up once
             int& occ = occ_by_quads[combine_stage_width(c) / 4];
             if (occ == 0) {
+                // the largest stage any row width takes (the attribute belongs to the kernel, whose
+                // launches for narrower rows ask for less)
                 cudaFuncSetAttribute(k_combine_split<Src, Epi, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(csmem));
+                                     static_cast<int>(combine_stage_bytes(kCombineCols)));
                 occ = max_blocks(k_combine_split<Src, Epi, true>, kCombineBlock, csmem);
             }
             const int64_t gb = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(occ) * num_sms(), groups));
